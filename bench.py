@@ -1,0 +1,347 @@
+"""Benchmark of the differential-attention forward hot path on one B300.
+
+One step = the whole hot path once:
+  * prefill: causal DiffAttn forward + GroupNorm + (1 - lambda_init) scale on
+    B=1, H=16, N=65536, d=64, dv=128 (bf16), one ``diffattn_fwd`` call;
+  * decode: split-KV decode on B=32, H=32, Nk=32768, d=64, dv=128 (bf16),
+    one ``diffattn_decode`` call (split pass + merge pass).
+
+``value`` is the prefill's algorithmic TFLOP/s (4 (d + dv) flops per unmasked
+query/key pair over the prefill launches' CUDA-event time); the decode's
+algorithmic GB/s (K1, K2 and V read once, q in, out) is reported beside it.
+Inputs are larger than L2 (768 MiB prefill, 16 GiB decode) and each step's
+decode streams 16 GiB, so nothing stays cached between timed iterations.
+
+``--impl reference`` times the fp64 CPU oracle instead (a bounded sample of
+prefill rows per step) on the host cores.
+Multi-GPU (torchrun): every rank runs its own independent problem of the
+same size (weak scaling, no data-path collective); time = max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DiffAttn fwd TFLOP/s (prefill) & KV GB/s (decode), % of B300 roofline"
+PREFILL = "long_64k"
+DECODE = "decode_32k"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["bf16_tflops"], p["bf16_tflops_sustained"], p["hbm_gbs"], "measured"
+    except Exception:
+        return 1800.0, 1400.0, 6400.0, "fallback"
+
+
+def traffic_from_profiles(kernel_key: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (its sha256 prefix is recorded beside it)."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
+    try:
+        text = open(path).read()
+        src = open(source, "rb").read()
+    except OSError:
+        return None
+    sha = hashlib.sha256(src).hexdigest()[:16]
+    m = re.search(rf"^\| {re.escape(kernel_key)} \| (\d+) \| ([0-9a-f]{{16}}) \|", text, re.M)
+    if not m or m.group(2) != sha:
+        return None
+    return int(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 300.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded),
+                "power_w_max": max(r[2] for r in rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(w, inp_cpu, rows):
+    import oracle
+    (o, y), dt = oracle.timed_fwd(*inp_cpu, w.lam, w.lam_init, causal=w.causal, eps=w.eps, rows=rows,
+                                  threads=os.cpu_count() or 1)
+    pairs = w.B * w.H * sum(min(w.Nk, r + (w.Nk - w.Nq) + 1) if w.causal else w.Nk for r in rows)
+    return 4 * (w.d + w.dv) * pairs, dt, pairs
+
+
+def sample_rows_uniform(N, n, seed):
+    import torch
+    g = torch.Generator().manual_seed(seed)
+    return sorted(set(torch.randint(0, N, (n,), generator=g).tolist()))
+
+
+def run_reference(args, world, rank):
+    """The fp64 oracle on the host cores: each step = a bounded row sample."""
+    import torch
+    from transformer_attention_07_b300.workloads import WORKLOADS, make_inputs
+    if rank != 0:
+        return 0
+    w = WORKLOADS[PREFILL]
+    inp = make_inputs(w, device="cpu")
+    cpu = [inp[k] for k in ("q1", "k1", "q2", "k2", "v")]
+    flops = secs = 0.0
+    for step in range(args.warmup + args.steps):
+        rows = sample_rows_uniform(w.Nq, args.ref_rows, 7000 + step)
+        f, dt, _ = oracle_sample(w, cpu, rows)
+        if step >= args.warmup:
+            flops += f
+            secs += dt
+    value = flops / secs / 1e12
+    sample = f"{args.ref_rows} seeded query rows x {w.H} heads of {PREFILL} per step"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{PREFILL}: causal prefill B1 H16 N65536 d64 dv128", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_cuda(args, world, rank, local):
+    import torch
+    import transformer_attention_07_b300 as da
+    from transformer_attention_07_b300.workloads import WORKLOADS, make_inputs
+
+    da.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wp, wd = WORKLOADS[args.prefill_workload], WORKLOADS[args.decode_workload]
+    do_pre, do_dec = args.only in ("all", "prefill"), args.only in ("all", "decode")
+    # Each rank its own independent problem (seed offset by rank).
+    pin = make_inputs(wp, device=dev, seed=wp.seed + 1000 * rank) if do_pre else None
+    din = make_inputs(wd, device=dev, seed=wd.seed + 1000 * rank) if do_dec else None
+    pout = torch.empty((wp.B, wp.H, wp.Nq, wp.dv), dtype=torch.bfloat16, device=dev) if do_pre else None
+    dout = torch.empty((wd.B, wd.H, 1, wd.dv), dtype=torch.bfloat16, device=dev) if do_dec else None
+    ws = torch.empty(da.decode_workspace_bytes(wd.B, wd.H, wd.Nk, wd.dv, 0), dtype=torch.uint8,
+                     device=dev) if do_dec else None
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        if do_pre:
+            da.fwd(pin["q1"], pin["k1"], pin["q2"], pin["k2"], pin["v"], wp.lam, wp.lam_init, causal=wp.causal,
+                   gamma=pin["gamma"], eps=wp.eps, out=pout, stream=stream)
+
+    def decode():
+        if do_dec:
+            da.decode(din["q1"], din["k1"], din["q2"], din["k2"], din["v"], wd.lam, wd.lam_init,
+                      gamma=din["gamma"], eps=wd.eps, workspace=ws, out=dout, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(vals):
+        if world == 1:
+            return vals
+        import torch.distributed as dist
+        t = torch.tensor(vals, device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return t.tolist()
+
+    for _ in range(args.warmup):
+        prefill()
+        decode()
+    torch.cuda.synchronize(dev)
+    if da.last_device_error() != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            prefill()
+            ev[s][1].record(stream)
+            decode()
+            ev[s][2].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    barrier()
+    if da.last_device_error() != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+    pre_ms = sum(ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps))
+    dec_ms = sum(ev[s][1].elapsed_time(ev[s][2]) for s in range(args.steps))
+    step_ms = ev[0][0].elapsed_time(ev[-1][2]) / args.steps
+    pre_ms, dec_ms, step_ms = max_over_ranks([pre_ms, dec_ms, step_ms])
+
+    # ------------------------------------------------ end to end: pinned host buffers in and out
+    e2e = None
+    names = ("q1", "k1", "q2", "k2", "v")
+    if do_pre and not args.no_e2e:
+        host = {k: pin[k].cpu().pin_memory() for k in names}
+        host_out = torch.empty(pout.shape, dtype=pout.dtype).pin_memory()
+
+        def e2e_step():
+            for k in names:
+                pin[k].copy_(host[k], non_blocking=True)
+            prefill()
+            host_out.copy_(pout, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        (e2e_ms,) = max_over_ranks([e0.elapsed_time(e1) / n_e2e])
+        e2e = {"value": wp.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": sum(host[k].numel() * host[k].element_size() for k in names),
+               "d2h_bytes_per_step": host_out.numel() * host_out.element_size(), "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peak_b, peak_s, peak_hbm, peak_src = load_peaks()
+    csrc = os.path.join(ROOT, "transformer_attention_07_b300", "csrc")
+    line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic"}
+    desc = []
+    if do_pre:
+        desc.append(f"{wp.name}: causal DiffAttn prefill B{wp.B} H{wp.H} N{wp.Nq} d{wp.d} dv{wp.dv}")
+    if do_dec:
+        desc.append(f"{wd.name}: split-KV decode B{wd.B} H{wd.H} Nk{wd.Nk} d{wd.d} dv{wd.dv}")
+    line["config"] = {"workload": " + ".join(desc), "parallelism": f"one independent problem per GPU x{world}",
+                      "l2": "inputs larger than L2 (prefill 768 MiB; decode streams 16 GiB per step)"}
+    if do_dec:
+        dec_gbs = wd.kv_bytes * args.steps * world / (dec_ms * 1e-3) / 1e9
+        dec_roof = {"bound": "hbm", "achieved": dec_gbs / world, "peak": peak_hbm, "unit": "GB/s",
+                    "frac": dec_gbs / world / peak_hbm, "peak_source": peak_src,
+                    "traffic": traffic_from_profiles(f"decode_split_kernel<64,128> {wd.name}",
+                                                     os.path.join(csrc, "decode_sm103a.cuh"))}
+        line["decode"] = {"value": dec_gbs, "unit": "GB/s", "ms": dec_ms / args.steps, "roofline": dec_roof}
+    if do_pre:
+        pre_tflops = wp.flops * args.steps * world / (pre_ms * 1e-3) / 1e12
+        line["value"], line["unit"] = pre_tflops, "TFLOP/s"
+        line["prefill_ms"] = pre_ms / args.steps
+        line["roofline"] = {"bound": "tensor", "achieved": pre_tflops / world, "peak": peak_b, "unit": "TFLOP/s",
+                            "frac": pre_tflops / world / peak_b, "peak_source": f"{peak_src} burst",
+                            "frac_of_sustained": pre_tflops / world / peak_s,
+                            "traffic": traffic_from_profiles(f"prefill_kernel<64,128,causal> {wp.name}",
+                                                             os.path.join(csrc, "prefill_sm103a.cuh"))}
+    else:
+        line["value"], line["unit"] = line["decode"]["value"], "GB/s"
+        line["roofline"] = line["decode"]["roofline"]
+    if e2e is not None:
+        line["e2e"] = e2e
+    line["gpu_launches"] = args.steps * ((1 if do_pre else 0) + (2 if do_dec else 0))
+    line["clocks"] = clk.summary()
+    line["wall_s_timed"] = wall
+    if do_pre and not args.no_cpu_baseline:
+        cpu = [pin[k].cpu() for k in names]
+        rows = sample_rows_uniform(wp.Nq, args.cpu_rows, 4242)
+        f, dt, _ = oracle_sample(wp, cpu, rows)
+        line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                "kind": "oracle", "seconds": dt,
+                                "sample": f"{len(rows)} seeded query rows x {wp.H} heads of {wp.name} "
+                                          "(fp64, every visible key of each row)"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="run one stage per step (profiling of a single kernel)")
+    ap.add_argument("--prefill-workload", default=PREFILL)
+    ap.add_argument("--decode-workload", default=DECODE)
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_cuda(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,126 @@
+/*
+ * diffattn.h — C ABI of the B300 (sm_103a) differential-attention forward.
+ *
+ * The operation (Differential Transformer pages):
+ *   "How does Differential Attention work to suppress noise and improve
+ *   long-context focus?" (iloveeagents.com), section "Mathematical Formula":
+ *       DiffAttn(Q,K,V) = ( softmax(Q1 K1^T / sqrt d) - lambda * softmax(Q2 K2^T / sqrt d) ) V
+ *   "Differential Transformer: How Noise-Canceling Attention Reinvents LLMs"
+ *   (llmbytes.dev), section "How Differential Attention Cancels Common-Mode
+ *   Noise", steps 2-4: two independent softmax maps, the lambda-weighted
+ *   subtraction, then GroupNorm of the multi-head output and a
+ *   (1 - lambda_init) scale.
+ *
+ * Readings fixed by this interface where the pages are silent:
+ *   - the logit scale is 1/sqrt(d), d = the Q/K head width;
+ *   - causal masking (optional) applies the same mask to both maps and is
+ *     bottom-right aligned: key j is visible to query i iff j <= i + Nk - Nq;
+ *   - GroupNorm: one group per head, statistics per token over that head's
+ *     dv channels, biased variance, eps inside the square root, per-channel
+ *     gain gamma[h*dv + c], no bias; the result is multiplied by
+ *     (1 - lambda_init).  lambda only weights the subtraction.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are device pointers, bf16 stored as 16-bit words, BHND row-major
+ *     and contiguous ([B][H][N][width], last dimension fastest), each 16-byte
+ *     aligned.  The caller owns all memory; the library never allocates device
+ *     memory and keeps no per-call state.
+ *   - Supported head widths: (d, dv) = (64, 128) or (32, 64).
+ *   - Arguments are validated on the host before anything is launched; on any
+ *     error nothing is launched and nothing is written.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *     the legacy default stream).  No entry point synchronises.
+ *   - A launch failure reported by the CUDA runtime returns DIFFATTN_ERR_CUDA.
+ *     Device-side waits are bounded: a wait that runs out records a code that
+ *     diffattn_last_device_error() returns, and the kernel exits.
+ */
+#ifndef DIFFATTN_H
+#define DIFFATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    DIFFATTN_OK = 0,
+    DIFFATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, bad eps/lambda */
+    DIFFATTN_ERR_UNSUPPORTED = 2, /* (d, dv) pair without a compiled kernel */
+    DIFFATTN_ERR_CUDA = 3,        /* the CUDA runtime reported an error at launch */
+    DIFFATTN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+    DIFFATTN_ERR_TIMEOUT = 5      /* a device-side wait ran out (see diffattn_last_device_error) */
+} diffattn_status;
+
+/*
+ * Prefill forward: y = (1 - lambda_init) * GroupNorm_h( (A1 - lambda A2) V ).
+ *   q1, q2      [B,H,Nq,d]  bf16
+ *   k1, k2      [B,H,Nk,d]  bf16
+ *   v           [B,H,Nk,dv] bf16
+ *   lambda      weight of the second map in the subtraction (any finite value)
+ *   lambda_init output scale is (1 - lambda_init) (any finite value)
+ *   causal      0 or 1; with 1, Nq <= Nk is required
+ *   gn_gamma    [H*dv] fp32 per-channel gain, or NULL for all ones
+ *   eps         GroupNorm epsilon, >= 0
+ *   out         [B,H,Nq,dv] bf16 result (round to nearest even)
+ * B, H or Nq equal to 0 is a valid empty problem (returns DIFFATTN_OK, no launch);
+ * Nk must be >= 1.
+ */
+int diffattn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                 float lambda, float lambda_init, int causal,
+                 int B, int H, int Nq, int Nk, int d, int dv,
+                 const float* gn_gamma, float eps, void* out, void* stream);
+
+/*
+ * As diffattn_fwd, and additionally writes the pre-norm output
+ * (A1 - lambda A2) V in fp32 to o_prenorm ([B,H,Nq,dv]) when it is not NULL.
+ */
+int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                    float lambda, float lambda_init, int causal,
+                    int B, int H, int Nq, int Nk, int d, int dv,
+                    const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream);
+
+/*
+ * Bytes of device workspace diffattn_decode needs for this shape and split
+ * count (num_splits = 0: enough for any split count the library chooses).
+ * Returns 0 for invalid sizes.
+ */
+size_t diffattn_decode_workspace_bytes(int B, int H, int Nk, int dv, int num_splits);
+
+/*
+ * Split-KV decode: one query per (b, h) against a key/value cache of Nk rows,
+ * no mask (the same operation as diffattn_fwd with Nq = 1, causal = 0).
+ *   q1, q2      [B,H,1,d] bf16;  k1, k2 [B,H,Nk,d] bf16;  v [B,H,Nk,dv] bf16
+ *   num_splits  0 = chosen by the library, else 1..64 key ranges per (b, h)
+ *   workspace   device scratch of >= diffattn_decode_workspace_bytes(...) bytes,
+ *               16-byte aligned; holds per-split partial softmax states.  It
+ *               needs no initialisation; concurrent calls need separate
+ *               workspaces.
+ *   out         [B,H,1,dv] bf16;  o_prenorm: NULL or [B,H,1,dv] fp32
+ * The key range of each (b, h) is cut into num_splits pieces; each piece
+ * yields the running maximum, normaliser and unnormalised output of both maps,
+ * and a second kernel merges the pieces (the associativity of the online
+ * softmax), forms O1/L1 - lambda O2/L2 and applies the GroupNorm and scale.
+ */
+int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                    float lambda, float lambda_init, int B, int H, int Nk, int d, int dv,
+                    const float* gn_gamma, float eps, int num_splits,
+                    void* workspace, size_t workspace_bytes,
+                    void* out, float* o_prenorm, void* stream);
+
+/* Static description of a status code. */
+const char* diffattn_status_string(int status);
+
+/*
+ * Reads and clears the device error word of the current device (synchronous:
+ * it waits for `stream`).  0 = no device-side error; otherwise a code naming
+ * the wait that ran out.  Returns -1 if the read itself failed.
+ */
+int diffattn_last_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIFFATTN_H */

@@ -1,0 +1,129 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every
+entry point include/diffattn.h declares, and rejects bad arguments on the host
+before any CUDA call (so these run on a machine without a device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import transformer_attention_07_b300 as da
+from transformer_attention_07_b300 import build as dabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "diffattn.h")
+
+OK, INVALID, UNSUPPORTED, CUDA, WORKSPACE, TIMEOUT = range(6)
+FAKE = ctypes.c_void_p(0x10000)       # 16-byte aligned, never dereferenced on error paths
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dabuild.build()
+    return da.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(diffattn_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    assert declared_functions() == sorted([
+        "diffattn_fwd", "diffattn_fwd_ex", "diffattn_decode_workspace_bytes", "diffattn_decode",
+        "diffattn_status_string", "diffattn_last_device_error"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_built_for_sm103a_only():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(dabuild.FLAGS)
+
+
+def fwd(lib, q=FAKE, out=FAKE, lam=0.5, lam_init=0.8, causal=0, B=1, H=1, Nq=4, Nk=4, d=64, dv=128,
+        gamma=None, eps=1e-5, pre=None):
+    return lib.diffattn_fwd_ex(q, q, q, q, q, lam, lam_init, causal, B, H, Nq, Nk, d, dv, gamma, eps, out, pre,
+                               None)
+
+
+def test_fwd_validation(lib):
+    assert fwd(lib, q=None) == INVALID
+    assert fwd(lib, out=None) == INVALID
+    assert fwd(lib, B=-1) == INVALID
+    assert fwd(lib, Nk=0) == INVALID
+    assert fwd(lib, causal=2) == INVALID
+    assert fwd(lib, causal=1, Nq=5, Nk=4) == INVALID
+    assert fwd(lib, eps=-1.0) == INVALID
+    assert fwd(lib, eps=float("nan")) == INVALID
+    assert fwd(lib, lam=float("inf")) == INVALID
+    assert fwd(lib, lam_init=float("nan")) == INVALID
+    assert fwd(lib, d=128, dv=128) == UNSUPPORTED
+    assert fwd(lib, d=64, dv=64) == UNSUPPORTED
+    assert fwd(lib, q=MISALIGNED) == INVALID
+    assert fwd(lib, pre=MISALIGNED) == INVALID
+    assert fwd(lib, gamma=ctypes.c_void_p(0x10002)) == INVALID
+    assert fwd(lib, H=70000) == INVALID
+
+
+def test_fwd_empty_problems_return_ok_without_launch(lib):
+    assert fwd(lib, B=0) == OK
+    assert fwd(lib, H=0) == OK
+    assert fwd(lib, Nq=0) == OK
+    assert fwd(lib, Nq=0, causal=1) == OK
+
+
+def test_decode_workspace_bytes(lib):
+    ws = lib.diffattn_decode_workspace_bytes
+    assert ws(32, 32, 32768, 128, 4) == 32 * 32 * 4 * 2 * (128 + 4) * 4
+    assert ws(2, 3, 100, 64, 0) == 2 * 3 * 32 * 2 * (64 + 4) * 4
+    assert ws(-1, 1, 1, 64, 0) == 0
+    assert ws(1, 1, 0, 64, 0) == 0
+    assert ws(1, 1, 10, 64, 65) == 0
+
+
+def dec(lib, q=FAKE, ws=FAKE, ws_bytes=1 << 20, splits=1, B=1, H=1, Nk=64, d=64, dv=128, out=FAKE, eps=1e-5):
+    return lib.diffattn_decode(q, q, q, q, q, 0.5, 0.8, B, H, Nk, d, dv, None, eps, splits, ws, ws_bytes, out,
+                               None, None)
+
+
+def test_decode_validation(lib):
+    assert dec(lib, q=None) == INVALID
+    assert dec(lib, out=None) == INVALID
+    assert dec(lib, Nk=0) == INVALID
+    assert dec(lib, splits=-1) == INVALID
+    assert dec(lib, splits=65) == INVALID
+    assert dec(lib, eps=-1.0) == INVALID
+    assert dec(lib, d=32, dv=128) == UNSUPPORTED
+    assert dec(lib, q=MISALIGNED) == INVALID
+    assert dec(lib, ws=None) == WORKSPACE
+    assert dec(lib, ws_bytes=16) == WORKSPACE
+    assert dec(lib, ws=ctypes.c_void_p(0x10004)) == INVALID
+    assert dec(lib, B=1 << 10, H=1 << 10, Nk=1 << 12) == INVALID   # > 2^31 cache rows
+    assert dec(lib, B=0) == OK
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert da.status_string(s)
+    assert da.status_string(99) == "unknown status"
+
+
+def test_binding_raises_without_cuda_tensors():
+    import torch
+    x = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        da.fwd(x, x, x, x, torch.zeros(1, 1, 4, 128, dtype=torch.bfloat16), 0.5, 0.8)
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "transformer_attention_07_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "oracle.cpp" not in text and "liboracle" not in text, f

@@ -1,0 +1,96 @@
+"""GPU parity of the split-KV decode path against the fp64 oracle (which
+computes decode as the forward pass with one query and no mask)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import transformer_attention_07_b300 as da
+from transformer_attention_07_b300.workloads import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_PRE = 1e-2
+TOL_OUT = 3e-2
+
+
+def random_cache(B, H, Nk, d, dv, seed, gamma=False):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    mk = lambda *s: torch.randn(s, generator=g, device="cuda").to(torch.bfloat16)
+    inp = {"q1": mk(B, H, 1, d), "k1": mk(B, H, Nk, d), "q2": mk(B, H, 1, d), "k2": mk(B, H, Nk, d),
+           "v": mk(B, H, Nk, dv)}
+    inp["gamma"] = (torch.rand(H * dv, generator=g, device="cuda") + 0.5) if gamma else None
+    return inp
+
+
+def gpu_decode(inp, lam, lam_init, splits=0, eps=1e-5):
+    B, H, _, _ = inp["q1"].shape
+    dv = inp["v"].shape[3]
+    pre = torch.full((B, H, 1, dv), float("nan"), dtype=torch.float32, device="cuda")
+    out = da.decode(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], lam, lam_init, gamma=inp.get("gamma"),
+                    eps=eps, num_splits=splits, o_prenorm=pre)
+    torch.cuda.synchronize()
+    assert da.last_device_error() == 0
+    return out, pre
+
+
+def oracle_decode(inp, lam, lam_init, eps=1e-5):
+    cpu = [inp[k].cpu() for k in ("q1", "k1", "q2", "k2", "v")]
+    g = inp.get("gamma")
+    g = None if g is None else g.double().cpu().numpy()
+    return oracle.diffattn_fwd(*cpu, lam, lam_init, causal=False, gamma=g, eps=eps)
+
+
+def check(out, pre, o_ref, y_ref):
+    out = out.float().cpu().numpy()
+    pre = pre.cpu().numpy()
+    assert np.isfinite(out).all() and np.isfinite(pre).all()
+    assert np.abs(pre - o_ref).max() <= TOL_PRE
+    assert np.abs(out - y_ref).max() <= TOL_OUT
+
+
+@pytest.mark.parametrize("B,H,Nk,d,dv,splits", [
+    (2, 3, 1000, 64, 128, 0),      # ragged last chunk, auto splits
+    (1, 2, 4096, 64, 128, 7),      # uneven split ranges
+    (3, 1, 33, 64, 128, 4),        # fewer keys than splits x 32: empty ranges
+    (1, 1, 1, 64, 128, 1),         # a single key
+    (2, 2, 2500, 32, 64, 0),       # d = 32 path
+    (1, 4, 70000, 64, 128, 64),    # many splits
+])
+def test_decode_matches_oracle(B, H, Nk, d, dv, splits):
+    inp = random_cache(B, H, Nk, d, dv, seed=Nk + splits, gamma=True)
+    out, pre = gpu_decode(inp, 0.6, 0.8, splits)
+    check(out, pre, *oracle_decode(inp, 0.6, 0.8))
+
+
+def test_decode_result_does_not_depend_on_split_count():
+    inp = random_cache(2, 2, 5000, 64, 128, seed=3)
+    _, ref = gpu_decode(inp, 0.6, 0.8, 1)
+    for s in (2, 5, 16, 33):
+        _, pre = gpu_decode(inp, 0.6, 0.8, s)
+        assert (pre - ref).abs().max().item() < 1e-5
+
+
+def test_decode_equals_prefill_with_one_query():
+    inp = random_cache(2, 3, 3000, 64, 128, seed=4, gamma=True)
+    _, pre_d = gpu_decode(inp, 0.45, 0.8)
+    pre_p = torch.empty_like(pre_d)
+    da.fwd(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], 0.45, 0.8, causal=False,
+           gamma=inp["gamma"], o_prenorm=pre_p)
+    torch.cuda.synchronize()
+    assert (pre_d - pre_p).abs().max().item() < 2e-3
+
+
+def test_decode_32k_sampled_heads():
+    """Full-size decode (B=32, H=32, Nk=32768): the whole batch runs on the
+    GPU; 24 seeded (b, h) heads are checked against the oracle."""
+    w = WORKLOADS["decode_32k"]
+    inp = make_inputs(w)
+    out, pre = gpu_decode(inp, w.lam, w.lam_init, eps=w.eps)
+    g = torch.Generator().manual_seed(w.seed)
+    heads = torch.randperm(w.B * w.H, generator=g)[:24].tolist()
+    sel = {k: torch.stack([inp[k][h // w.H, h % w.H] for h in heads])[:, None] for k in ("q1", "k1", "q2", "k2", "v")}
+    o_ref, y_ref = oracle_decode(sel, w.lam, w.lam_init, w.eps)
+    out_s = torch.stack([out[h // w.H, h % w.H] for h in heads])[:, None]
+    pre_s = torch.stack([pre[h // w.H, h % w.H] for h in heads])[:, None]
+    check(out_s, pre_s, o_ref, y_ref)

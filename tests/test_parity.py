@@ -1,0 +1,165 @@
+"""GPU parity: the CUDA library against the fp64 oracle on the same bf16 bits.
+
+Tolerances (max-abs, bf16 inputs, fp32 accumulation): 1e-2 on the pre-norm
+output (A1 - lambda A2) V, 3e-2 on the normalised, scaled bf16 output.
+
+Small problems are compared element by element over every row (sizes that
+span several 128-row / 128-key tiles and end in ragged tails); the full-size
+workloads are compared on sampled rows (first and last rows plus seeded
+random rows, and every needle row of the cancellation workload) that the
+oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import transformer_attention_07_b300 as da
+from transformer_attention_07_b300.workloads import WORKLOADS, make_inputs, needle_rows, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+TOL_PRE = 1e-2
+TOL_OUT = 3e-2
+
+
+def gpu_fwd(inp, lam, lam_init, causal, eps=1e-5):
+    B, H, Nq, _ = inp["q1"].shape
+    dv = inp["v"].shape[3]
+    pre = torch.full((B, H, Nq, dv), float("nan"), dtype=torch.float32, device="cuda")
+    out = da.fwd(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], lam, lam_init, causal=causal,
+                 gamma=inp.get("gamma"), eps=eps, o_prenorm=pre)
+    torch.cuda.synchronize()
+    assert da.last_device_error() == 0
+    return out, pre
+
+
+def oracle_fwd(inp, lam, lam_init, causal, eps=1e-5, rows=None):
+    cpu = [inp[k].cpu() for k in ("q1", "k1", "q2", "k2", "v")]
+    g = inp.get("gamma")
+    g = None if g is None else g.double().cpu().numpy()
+    return oracle.diffattn_fwd(*cpu, lam, lam_init, causal=causal, gamma=g, eps=eps, rows=rows)
+
+
+def compare(out, pre, o_ref, y_ref, rows=None):
+    out = out.float().cpu().numpy()
+    pre = pre.cpu().numpy()
+    if rows is not None:
+        out, pre = out[:, :, rows], pre[:, :, rows]
+    assert np.isfinite(out).all() and np.isfinite(pre).all()
+    e_pre = np.abs(pre - o_ref).max()
+    e_out = np.abs(out - y_ref).max()
+    assert e_pre <= TOL_PRE, f"pre-norm max-abs error {e_pre}"
+    assert e_out <= TOL_OUT, f"normalised max-abs error {e_out}"
+    return e_pre, e_out
+
+
+def random_inputs(B, H, Nq, Nk, d, dv, seed, gamma=True):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    mk = lambda *s: torch.randn(s, generator=g, device="cuda").to(torch.bfloat16)
+    inp = {"q1": mk(B, H, Nq, d), "k1": mk(B, H, Nk, d), "q2": mk(B, H, Nq, d), "k2": mk(B, H, Nk, d),
+           "v": mk(B, H, Nk, dv)}
+    inp["gamma"] = (torch.rand(H * dv, generator=g, device="cuda") + 0.5) if gamma else None
+    return inp
+
+
+# ------------------------------------------------------------------ full compares
+
+def test_tiny_noncausal_full():
+    w = WORKLOADS["tiny_noncausal"]
+    inp = make_inputs(w)
+    out, pre = gpu_fwd(inp, w.lam, w.lam_init, w.causal, w.eps)
+    compare(out, pre, *oracle_fwd(inp, w.lam, w.lam_init, w.causal, w.eps))
+
+
+def test_causal_2k_full():
+    w = WORKLOADS["causal_2k"]
+    inp = make_inputs(w)
+    out, pre = gpu_fwd(inp, w.lam, w.lam_init, w.causal, w.eps)
+    compare(out, pre, *oracle_fwd(inp, w.lam, w.lam_init, w.causal, w.eps))
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,dv,causal", [
+    (1, 2, 300, 300, 64, 128, True),     # ragged tail, 3 tiles, diagonal masking
+    (2, 1, 200, 333, 64, 128, False),    # ragged queries and keys
+    (1, 2, 130, 400, 64, 128, True),     # Nq < Nk: bottom-right causal alignment
+    (1, 1, 1, 77, 64, 128, False),       # single query
+    (1, 1, 5, 5, 64, 128, True),         # less than one tile
+    (1, 3, 257, 257, 32, 64, True),      # d = 32 path, ragged
+    (1, 1, 129, 1000, 32, 64, False),    # d = 32, many key tiles
+    (3, 2, 512, 512, 64, 128, True),     # whole tiles, several batches
+])
+def test_ragged_shapes_full(B, H, Nq, Nk, d, dv, causal):
+    inp = random_inputs(B, H, Nq, Nk, d, dv, seed=Nq * 7 + Nk)
+    out, pre = gpu_fwd(inp, 0.6, 0.8, causal)
+    compare(out, pre, *oracle_fwd(inp, 0.6, 0.8, causal))
+
+
+@pytest.mark.parametrize("lam", [0.0, 1.0, -0.5, 1.5])
+def test_lambda_edge_values(lam):
+    inp = random_inputs(1, 2, 256, 256, 64, 128, seed=5)
+    out, pre = gpu_fwd(inp, lam, 0.8, True)
+    compare(out, pre, *oracle_fwd(inp, lam, 0.8, True))
+
+
+def test_large_logits_trigger_rescaling():
+    """Logits spread over ~60 units (log2 domain) so the running max grows by
+    more than 2^8 across tiles: exercises the accumulator rescale."""
+    inp = random_inputs(1, 2, 512, 512, 64, 128, seed=6)
+    ramp = torch.linspace(0, 4, 512, device="cuda")[None, None, :, None]
+    inp["k1"] = (inp["k1"].float() + ramp * inp["q1"].float().mean(2, keepdim=True)).to(torch.bfloat16)
+    inp["q1"] = (inp["q1"].float() * 3).to(torch.bfloat16)
+    out, pre = gpu_fwd(inp, 0.5, 0.8, True)
+    compare(out, pre, *oracle_fwd(inp, 0.5, 0.8, True))
+
+
+# ------------------------------------------------------------------ GPU invariants
+
+def test_gpu_affine_in_lambda():
+    inp = random_inputs(1, 2, 384, 384, 64, 128, seed=7)
+    _, p0 = gpu_fwd(inp, 0.0, 0.8, True)
+    _, p1 = gpu_fwd(inp, 1.0, 0.8, True)
+    _, pl = gpu_fwd(inp, 0.3, 0.8, True)
+    assert (pl - (p0 - 0.3 * (p0 - p1))).abs().max().item() < 1e-4
+
+
+def test_gpu_constant_one_value_column_gives_one_minus_lambda():
+    inp = random_inputs(2, 2, 300, 300, 64, 128, seed=8)
+    inp["v"][..., 0] = 1.0
+    for causal in (False, True):
+        _, pre = gpu_fwd(inp, 0.7, 0.8, causal)
+        assert (pre[..., 0] - 0.3).abs().max().item() < 1e-4
+
+
+def test_gpu_causal_first_row_is_scaled_first_value():
+    inp = random_inputs(2, 3, 256, 256, 64, 128, seed=9)
+    _, pre = gpu_fwd(inp, 0.25, 0.8, True)
+    ref = 0.75 * inp["v"][:, :, 0].float()
+    assert (pre[:, :, 0] - ref).abs().max().item() < 1e-5
+
+
+def test_gpu_identical_maps_with_lambda_one_cancel_exactly():
+    inp = random_inputs(1, 2, 300, 300, 64, 128, seed=10)
+    inp["q2"], inp["k2"] = inp["q1"].clone(), inp["k1"].clone()
+    out, pre = gpu_fwd(inp, 1.0, 0.8, True)
+    assert pre.abs().max().item() == 0.0
+    assert out.float().abs().max().item() == 0.0
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled rows)
+
+def test_cancel_8k_sampled_rows():
+    w = WORKLOADS["cancel_8k"]
+    inp = make_inputs(w)
+    out, pre = gpu_fwd(inp, w.lam, w.lam_init, w.causal, w.eps)
+    rows = sorted(set(sample_rows(w.Nq, w.seed, n_random=192)) | set(needle_rows(w.Nq)[::4]))
+    compare(out, pre, *oracle_fwd(inp, w.lam, w.lam_init, w.causal, w.eps, rows=rows), rows=rows)
+
+
+@pytest.mark.parametrize("name", ["long_64k", "long_128k"])
+def test_long_context_sampled_rows(name):
+    w = WORKLOADS[name]
+    inp = make_inputs(w)
+    out, pre = gpu_fwd(inp, w.lam, w.lam_init, w.causal, w.eps)
+    rows = sample_rows(w.Nq, w.seed, n_random=48, edge=16)
+    compare(out, pre, *oracle_fwd(inp, w.lam, w.lam_init, w.causal, w.eps, rows=rows), rows=rows)

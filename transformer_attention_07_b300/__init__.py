@@ -1,0 +1,156 @@
+"""B300 (sm_103a) differential-attention forward: Python binding of libdiffattn.so.
+
+The functions here marshal torch CUDA tensors into the C ABI declared in
+``include/diffattn.h`` (pointers, sizes, the current stream) and do no
+arithmetic: every step of the forward pass runs in the library's kernels.
+If the shared library has not been built, every call raises; there is no
+fallback implementation.
+
+What the library computes (Differential Transformer pages — the DiffAttn
+formula of the iloveeagents.com Q&A, "Mathematical Formula", and steps 2-4 of
+llmbytes.dev "How Differential Attention Cancels Common-Mode Noise"):
+
+    y = (1 - lambda_init) * GroupNorm_h( (softmax(Q1 K1^T/sqrt d) - lambda softmax(Q2 K2^T/sqrt d)) V )
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "fwd", "decode", "decode_workspace_bytes", "status_string", "last_device_error",
+    "load", "LIB_PATH", "DiffAttnError", "SUPPORTED_WIDTHS",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdiffattn.so")
+SUPPORTED_WIDTHS = ((64, 128), (32, 64))
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_WORKSPACE, ERR_TIMEOUT = range(6)
+
+_lib = None
+
+
+class DiffAttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def load():
+    """Load libdiffattn.so (built by ``python -m transformer_attention_07_b300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -m transformer_attention_07_b300.build` "
+            "(there is no non-CUDA implementation)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.diffattn_fwd.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp, vp]
+    lib.diffattn_fwd.restype = i32
+    lib.diffattn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32, vp, f32,
+                                    vp, vp, vp]
+    lib.diffattn_fwd_ex.restype = i32
+    lib.diffattn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.diffattn_decode_workspace_bytes.restype = sz
+    lib.diffattn_decode.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, vp, f32, i32, vp, sz,
+                                    vp, vp, vp]
+    lib.diffattn_decode.restype = i32
+    lib.diffattn_status_string.argtypes = [i32]
+    lib.diffattn_status_string.restype = ctypes.c_char_p
+    lib.diffattn_last_device_error.argtypes = [vp]
+    lib.diffattn_last_device_error.restype = i32
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().diffattn_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_bf16(name, t, ndim=4):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be a CUDA bf16 tensor")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor [B,H,N,width]")
+
+
+def _gamma(gamma, H, dv):
+    import torch
+    if gamma is None:
+        return None
+    if not gamma.is_cuda or gamma.dtype != torch.float32 or not gamma.is_contiguous() or gamma.numel() != H * dv:
+        raise ValueError("gamma must be a contiguous CUDA float32 tensor with H*dv entries")
+    return gamma
+
+
+def fwd(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps=1e-5, out=None, o_prenorm=None,
+        stream=None):
+    """Prefill forward.  q1,q2 [B,H,Nq,d]; k1,k2 [B,H,Nk,d]; v [B,H,Nk,dv] (CUDA bf16).
+
+    Returns ``out`` (bf16 [B,H,Nq,dv], allocated if not given).  If
+    ``o_prenorm`` (fp32 [B,H,Nq,dv]) is given, the pre-norm output is written
+    there too.  Asynchronous on ``stream`` (default: torch's current stream)."""
+    import torch
+    for n, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2), ("v", v)):
+        _check_bf16(n, t)
+    B, H, Nq, d = q1.shape
+    Nk, dv = k1.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, H, Nq, dv), dtype=torch.bfloat16, device=q1.device)
+    g = _gamma(gamma, H, dv)
+    rc = load().diffattn_fwd_ex(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), float(lam), float(lam_init),
+                                int(bool(causal)), B, H, Nq, Nk, d, dv, _ptr(g), float(eps), _ptr(out),
+                                _ptr(o_prenorm), _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_fwd")
+    return out
+
+
+def decode_workspace_bytes(B, H, Nk, dv, num_splits=0) -> int:
+    return int(load().diffattn_decode_workspace_bytes(B, H, Nk, dv, num_splits))
+
+
+def decode(q1, k1, q2, k2, v, lam, lam_init, gamma=None, eps=1e-5, num_splits=0, workspace=None, out=None,
+           o_prenorm=None, stream=None):
+    """Split-KV decode: q1,q2 [B,H,1,d]; k1,k2 [B,H,Nk,d]; v [B,H,Nk,dv] (CUDA bf16).
+
+    ``workspace`` is a CUDA tensor of at least ``decode_workspace_bytes`` bytes
+    (allocated here if not given).  Returns ``out`` (bf16 [B,H,1,dv])."""
+    import torch
+    for n, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2), ("v", v)):
+        _check_bf16(n, t)
+    B, H, Nq, d = q1.shape
+    if Nq != 1:
+        raise ValueError("decode takes one query per (b, h)")
+    Nk, dv = k1.shape[2], v.shape[3]
+    nbytes = decode_workspace_bytes(B, H, Nk, dv, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q1.device)
+    if out is None:
+        out = torch.empty((B, H, 1, dv), dtype=torch.bfloat16, device=q1.device)
+    g = _gamma(gamma, H, dv)
+    rc = load().diffattn_decode(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), float(lam), float(lam_init),
+                                B, H, Nk, d, dv, _ptr(g), float(eps), int(num_splits), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _ptr(out), _ptr(o_prenorm),
+                                _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_decode")
+    return out
+
+
+def last_device_error(stream=None) -> int:
+    """Read and clear the device error word (synchronises ``stream``)."""
+    return int(load().diffattn_last_device_error(_stream(stream)))

@@ -1,0 +1,150 @@
+// C ABI of the differential-attention library (declared in include/diffattn.h).
+// Each entry point checks every argument on the host first and launches
+// nothing when one is wrong; the launchers in kernels.cu do the rest.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/diffattn.h"
+#include "launch.h"
+
+namespace {
+
+constexpr int kMaxAutoSplits = 32;
+constexpr int kMaxSplits = 64;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+bool supported_widths(int d, int dv) { return (d == 64 && dv == 128) || (d == 32 && dv == 64); }
+
+int from_launch(int s) {
+    if (s == diffattn::LAUNCH_OK) return DIFFATTN_OK;
+    if (s == diffattn::LAUNCH_ERR_UNSUPPORTED) return DIFFATTN_ERR_UNSUPPORTED;
+    return DIFFATTN_ERR_CUDA;
+}
+
+// Per-call scalars shared by both entry points.
+int check_scalars(float lambda, float lambda_init, float eps) {
+    if (!std::isfinite(lambda) || !std::isfinite(lambda_init)) return DIFFATTN_ERR_INVALID_ARG;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return DIFFATTN_ERR_INVALID_ARG;
+    return DIFFATTN_OK;
+}
+
+// A BHND tensor of this shape must be describable by a 4-D tensor map:
+// every byte stride below 2^40.
+bool fits_tensor_map(int64_t H, int64_t N, int64_t W) { return H * N * W * 2 < (int64_t(1) << 40); }
+
+size_t workspace_for(int B, int H, int dv, int splits) {
+    return (size_t)B * (size_t)H * (size_t)splits * 2u * (size_t)(dv + 4) * sizeof(float);
+}
+
+// Key ranges per (b, h): enough CTAs to fill the GPU in whole waves, and at
+// least 512 keys per range.
+int choose_splits(int64_t heads, int Nk, int sms) {
+    const int by_keys = (int)((Nk + 511) / 512);
+    const int cap = by_keys < kMaxAutoSplits ? (by_keys < 1 ? 1 : by_keys) : kMaxAutoSplits;
+    int best = 1;
+    double best_eff = -1.0;
+    for (int s = 1; s <= cap; ++s) {
+        const double ctas = (double)heads * s;
+        const double waves = std::ceil(ctas / sms);
+        const double eff = ctas / (waves * sms);
+        if (eff > best_eff + 0.01) {
+            best = s;
+            best_eff = eff;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+extern "C" {
+
+int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                    float lambda, float lambda_init, int causal, int B, int H, int Nq, int Nk, int d, int dv,
+                    const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;   // grid y/z limits
+    if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
+    diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
+                            gn_gamma, out, o_prenorm};
+    return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+int diffattn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, float lambda,
+                 float lambda_init, int causal, int B, int H, int Nq, int Nk, int d, int dv, const float* gn_gamma,
+                 float eps, void* out, void* stream) {
+    return diffattn_fwd_ex(q1, k1, q2, k2, v, lambda, lambda_init, causal, B, H, Nq, Nk, d, dv, gn_gamma, eps, out,
+                           nullptr, stream);
+}
+
+size_t diffattn_decode_workspace_bytes(int B, int H, int Nk, int dv, int num_splits) {
+    if (B < 0 || H < 0 || Nk < 1 || dv < 1 || num_splits < 0 || num_splits > kMaxSplits) return 0;
+    return workspace_for(B, H, dv, num_splits == 0 ? kMaxAutoSplits : num_splits);
+}
+
+int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, float lambda,
+                    float lambda_init, int B, int H, int Nk, int d, int dv, const float* gn_gamma, float eps,
+                    int num_splits, void* workspace, size_t workspace_bytes, void* out, float* o_prenorm,
+                    void* stream) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (num_splits < 0 || num_splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    // The key caches are addressed as one [B*H*Nk, d] matrix with 32-bit rows.
+    if ((int64_t)B * H * Nk >= (int64_t(1) << 31) - 64) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H == 0) return DIFFATTN_OK;
+    int splits = num_splits;
+    if (splits == 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+            return DIFFATTN_ERR_CUDA;
+        splits = choose_splits((int64_t)B * H, Nk, sms);
+    }
+    if (!workspace || workspace_bytes < workspace_for(B, H, dv, splits)) return DIFFATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DIFFATTN_ERR_INVALID_ARG;
+    const int per = (Nk + splits - 1) / splits;
+    const int keys_per_split = (per + 31) / 32 * 32;
+    diffattn::DecodeArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, B, H, Nk, d, dv,
+                           splits, keys_per_split, gn_gamma, static_cast<float*>(workspace), out, o_prenorm};
+    return from_launch(diffattn::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+const char* diffattn_status_string(int status) {
+    switch (status) {
+        case DIFFATTN_OK: return "ok";
+        case DIFFATTN_ERR_INVALID_ARG: return "invalid argument";
+        case DIFFATTN_ERR_UNSUPPORTED: return "unsupported head widths (d, dv)";
+        case DIFFATTN_ERR_CUDA: return "CUDA runtime error";
+        case DIFFATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case DIFFATTN_ERR_TIMEOUT: return "device-side wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int diffattn_last_device_error(void* stream) {
+    int v = 0;
+    if (diffattn::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &v) != diffattn::LAUNCH_OK)
+        return -1;
+    return v;
+}
+
+}  // extern "C"

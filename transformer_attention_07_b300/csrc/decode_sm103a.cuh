@@ -1,0 +1,329 @@
+// Split-KV differential-attention decode for sm_103a: one query per (b, h)
+// against a cache of Nk keys, no mask.  HBM-bound: every K1, K2 and V byte is
+// read exactly once.
+//
+// Pass 1 (decode_split_kernel), grid (splits, H, B): a CTA owns one key range
+// of one (b, h).  A producer warp streams 32-key chunks of K1 and K2 (tiled
+// TMA, 128/64-byte swizzle so that lane-per-key reads are conflict-free) and
+// of V (bulk copy) into a 12-16 stage shared-memory ring.  Eight consumer
+// warps take chunks round-robin; in a warp, lane t scores key t against q1
+// and q2, the warp keeps one online-softmax state per map (max m_r, per-lane
+// partial normaliser l_r, unnormalised output O_r spread over the lanes by dv
+// column) and accumulates O_r += p_r[j] v_j with the probabilities broadcast
+// by shuffle.  The warps' states are merged in shared memory and one partial
+// (m_r, l_r, O_r) per map is written to the workspace.
+//
+// Pass 2 (decode_merge_kernel), one warp per (b, h): merges the split
+// partials with warp shuffles — M = max m_s, L = sum l_s 2^(m_s - M),
+// O = sum O_s 2^(m_s - M) — the same associative rescaling the online
+// softmax uses, then o = O1/L1 - lambda O2/L2, GroupNorm over dv, gain and
+// (1 - lambda_init), bf16 store.  (Differential Transformer pages: the
+// DiffAttn formula of the iloveeagents.com Q&A, "Mathematical Formula";
+// steps 2-4 of llmbytes.dev "How Differential Attention Cancels Common-Mode
+// Noise".)
+#pragma once
+
+#include "sm103_ptx.cuh"
+
+namespace diffattn {
+
+struct DecodeParams {
+    const uint16_t* q1;
+    const uint16_t* q2;
+    const uint16_t* v;
+    int B, H, Nk, S;
+    int keys_per_split;   // multiple of 32
+    float scale_log2;     // log2(e) / sqrt(d)
+    float* ws;            // [B*H*S][2][DV + 4] partials: m, l, pad, pad, O[DV]
+};
+
+struct MergeParams {
+    int B, H, S;
+    float lambda, lambda_init, eps;
+    const float* ws;
+    const float* gamma;   // [H*DV] or null
+    uint16_t* out;        // bf16 [B*H, DV]
+    float* o_prenorm;     // fp32 [B*H, DV] or null
+};
+
+template <int D, int DV>
+struct DecodeLayout {
+    static constexpr int KC = 32;                       // keys per chunk (one per lane)
+    static constexpr int NCW = 8;                       // consumer warps
+    static constexpr int THREADS = (NCW + 1) * 32;      // + producer warp
+    static constexpr uint32_t K_BYTES = KC * D * 2;
+    static constexpr uint32_t V_BYTES = KC * DV * 2;
+    static constexpr uint32_t STAGE = 2 * K_BYTES + V_BYTES;
+    static constexpr int NST = (D == 64) ? 12 : 16;
+    static constexpr uint32_t OFF_RING = 0;
+    static constexpr int PART = DV + 4;                 // floats per (map) partial
+    static constexpr uint32_t OFF_RED = NST * STAGE;    // NCW x 2 x PART floats
+    static constexpr uint32_t OFF_BAR = OFF_RED + NCW * 2 * PART * 4;
+    static constexpr uint32_t USED = OFF_BAR + 2 * NST * 8;
+    static constexpr uint32_t SMEM_BYTES = USED + 1024;
+    static constexpr uint32_t SWZ_BYTES = (D == 64) ? 128 : 64;   // K row = swizzle span
+    static_assert(USED + 1024 <= 227u * 1024u, "shared memory");
+    static_assert(STAGE % 1024 == 0, "stage alignment");
+};
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Dot product of a bf16 key row held in swizzled shared memory with q (fp32
+// registers).  Row r of the tile starts at r*2D bytes; the 16-byte chunk c of
+// the row sits at chunk position c ^ ((row byte offset >> 7) & (span/16 - 1)).
+template <int D>
+__device__ __forceinline__ float dot_row_swizzled(const uint8_t* tile, int r, const float (&q)[D]) {
+    constexpr int RB = D * 2;
+    constexpr int MASK = (D == 64) ? 7 : 3;
+    const int sw = ((r * RB) >> 7) & MASK;
+    const uint8_t* row = tile + r * RB;
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+        const uint4 kk = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+        acc0 = fmaf(q[8 * c + 0], bf16lo_to_f32(kk.x), acc0);
+        acc1 = fmaf(q[8 * c + 1], bf16hi_to_f32(kk.x), acc1);
+        acc0 = fmaf(q[8 * c + 2], bf16lo_to_f32(kk.y), acc0);
+        acc1 = fmaf(q[8 * c + 3], bf16hi_to_f32(kk.y), acc1);
+        acc0 = fmaf(q[8 * c + 4], bf16lo_to_f32(kk.z), acc0);
+        acc1 = fmaf(q[8 * c + 5], bf16hi_to_f32(kk.z), acc1);
+        acc0 = fmaf(q[8 * c + 6], bf16lo_to_f32(kk.w), acc0);
+        acc1 = fmaf(q[8 * c + 7], bf16hi_to_f32(kk.w), acc1);
+    }
+    return acc0 + acc1;
+}
+
+template <int D, int DV>
+__global__ void __launch_bounds__(DecodeLayout<D, DV>::THREADS, 1)
+decode_split_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
+                    const DecodeParams p) {
+    using L = DecodeLayout<D, DV>;
+    constexpr int CPL = DV / 32;   // dv columns per lane
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const size_t bh = (size_t)b * p.H + h;
+    const int key_begin = s * p.keys_per_split;
+    const int key_end = min(p.Nk, key_begin + p.keys_per_split);
+    const int nkeys = max(0, key_end - key_begin);
+    const int nchunks = (nkeys + L::KC - 1) / L::KC;
+
+    auto full = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)i; };
+    auto empty = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)(L::NST + i); };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < L::NST; ++i) {
+            mbar_init(full(i), 1);
+            mbar_init(empty(i), 1);
+        }
+        fence_mbar_init();
+        prefetch_tensormap(&tm_k1);
+        prefetch_tensormap(&tm_k2);
+    }
+    __syncthreads();
+
+    float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
+
+    if (warp == L::NCW) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const int krow0 = (int)(bh * (size_t)p.Nk) + key_begin;   // row in the [B*H*Nk, D] view
+            int issued = 0;
+            for (int c = 0; c < nchunks; ++c) {
+                const int st = c % L::NST;
+                if (!mbar_wait(empty(st), ((c / L::NST) & 1) ^ 1, ERR_SITE_DECODE_PRODUCER)) break;
+                const int k0 = key_begin + c * L::KC;
+                const int rows = min(L::KC, key_end - k0);
+                const uint32_t base = sb + L::OFF_RING + (uint32_t)st * L::STAGE;
+                mbar_arrive_expect_tx(full(st), 2 * L::K_BYTES + (uint32_t)rows * DV * 2);
+                tma_load_4d(base, &tm_k1, full(st), 0, krow0 + c * L::KC, 0, 0);
+                tma_load_4d(base + L::K_BYTES, &tm_k2, full(st), 0, krow0 + c * L::KC, 0, 0);
+                bulk_load(base + 2 * L::K_BYTES, p.v + (bh * (size_t)p.Nk + k0) * DV, (uint32_t)rows * DV * 2,
+                          full(st));
+                ++issued;
+            }
+            for (int st = 0; st < L::NST && st < issued; ++st) {
+                const int last = st + ((issued - 1 - st) / L::NST) * L::NST;
+                mbar_wait(full(st), (last / L::NST) & 1, ERR_SITE_DECODE_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ consumers
+        float q1[D], q2[D];
+#pragma unroll
+        for (int i = 0; i < D; ++i) {
+            q1[i] = __uint_as_float((uint32_t)p.q1[bh * D + i] << 16);
+            q2[i] = __uint_as_float((uint32_t)p.q2[bh * D + i] << 16);
+        }
+        float m1 = -INFINITY, m2 = -INFINITY, l1 = 0.f, l2 = 0.f;
+        float o1[CPL], o2[CPL];
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) o1[i] = o2[i] = 0.f;
+        const float sl2 = p.scale_log2;
+        for (int c = warp; c < nchunks; c += L::NCW) {
+            const int st = c % L::NST;
+            bool ok = mbar_wait(full(st), (c / L::NST) & 1, ERR_SITE_DECODE_CONSUMER);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            const uint8_t* base = smem + L::OFF_RING + (size_t)st * L::STAGE;
+            const int rows = min(L::KC, key_end - (key_begin + c * L::KC));
+            const bool valid = lane < rows;
+            float s1 = dot_row_swizzled<D>(base, lane, q1) * sl2;
+            float s2 = dot_row_swizzled<D>(base + L::K_BYTES, lane, q2) * sl2;
+            if (!valid) s1 = s2 = -INFINITY;
+            const float n1 = fmaxf(m1, warp_max(s1));
+            const float n2 = fmaxf(m2, warp_max(s2));
+            const float a1 = fast_exp2(m1 - n1), a2 = fast_exp2(m2 - n2);   // m = -inf -> 0
+            const float p1 = fast_exp2(s1 - n1), p2 = fast_exp2(s2 - n2);
+            m1 = n1;
+            m2 = n2;
+            l1 = l1 * a1 + p1;
+            l2 = l2 * a2 + p2;
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                o1[i] *= a1;
+                o2[i] *= a2;
+            }
+            const uint8_t* vt = base + 2 * L::K_BYTES;
+            for (int j = 0; j < rows; ++j) {
+                const float pj1 = __shfl_sync(0xffffffffu, p1, j);
+                const float pj2 = __shfl_sync(0xffffffffu, p2, j);
+                const uint8_t* vr = vt + (size_t)j * DV * 2 + lane * CPL * 2;
+                float vv[CPL];
+                if constexpr (CPL == 4) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(vr);
+                    vv[0] = bf16lo_to_f32(w.x); vv[1] = bf16hi_to_f32(w.x);
+                    vv[2] = bf16lo_to_f32(w.y); vv[3] = bf16hi_to_f32(w.y);
+                } else {
+                    const uint32_t w = *reinterpret_cast<const uint32_t*>(vr);
+                    vv[0] = bf16lo_to_f32(w); vv[1] = bf16hi_to_f32(w);
+                }
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) {
+                    o1[i] = fmaf(pj1, vv[i], o1[i]);
+                    o2[i] = fmaf(pj2, vv[i], o2[i]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(st));
+        }
+        // Per-warp state -> shared memory.
+        l1 = warp_sum(l1);
+        l2 = warp_sum(l2);
+        float* w1 = red + (warp * 2 + 0) * L::PART;
+        float* w2 = red + (warp * 2 + 1) * L::PART;
+        if (lane == 0) {
+            w1[0] = m1; w1[1] = l1;
+            w2[0] = m2; w2[1] = l2;
+        }
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            w1[4 + lane * CPL + i] = o1[i];
+            w2[4 + lane * CPL + i] = o2[i];
+        }
+        named_barrier_sync(1, L::NCW * 32);
+        // Merge the warps: thread t -> (map t / DV, column t % DV).
+        for (int t = threadIdx.x; t < 2 * DV; t += L::NCW * 32) {
+            const int r = t / DV, col = t % DV;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < L::NCW; ++w) M = fmaxf(M, red[(w * 2 + r) * L::PART]);
+            float Ls = 0.f, Os = 0.f;
+            if (M != -INFINITY) {
+#pragma unroll
+                for (int w = 0; w < L::NCW; ++w) {
+                    const float* src = red + (w * 2 + r) * L::PART;
+                    const float e = fast_exp2(src[0] - M);
+                    Ls = fmaf(src[1], e, Ls);
+                    Os = fmaf(src[4 + col], e, Os);
+                }
+            }
+            float* dst = p.ws + ((bh * p.S + s) * 2 + r) * L::PART;
+            dst[4 + col] = Os;
+            if (col == 0) {
+                dst[0] = M;
+                dst[1] = Ls;
+            }
+        }
+    }
+}
+
+template <int DV>
+__global__ void __launch_bounds__(128)
+decode_merge_kernel(const MergeParams p) {
+    constexpr int PART = DV + 4;
+    constexpr int CPL = DV / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const size_t bh = (size_t)blockIdx.x * 4 + warp;
+    if (bh >= (size_t)p.B * p.H) return;
+    const int h = (int)(bh % p.H);
+    const float* part = p.ws + bh * p.S * 2 * PART;
+    float O[2][CPL], Lr[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float M = -INFINITY;
+        for (int s = lane; s < p.S; s += 32) M = fmaxf(M, part[(s * 2 + r) * PART]);
+        M = warp_max(M);
+        float Ls = 0.f;
+        for (int s = lane; s < p.S; s += 32) {
+            const float m = part[(s * 2 + r) * PART];
+            if (m != -INFINITY) Ls = fmaf(part[(s * 2 + r) * PART + 1], fast_exp2(m - M), Ls);
+        }
+        Lr[r] = warp_sum(Ls);
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) O[r][i] = 0.f;
+        for (int s = 0; s < p.S; ++s) {
+            const float* src = part + (s * 2 + r) * PART;
+            const float m = src[0];
+            if (m == -INFINITY) continue;
+            const float e = fast_exp2(m - M);
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) O[r][i] = fmaf(src[4 + lane * CPL + i], e, O[r][i]);
+        }
+    }
+    const float inv1 = 1.0f / Lr[0], inv2 = p.lambda / Lr[1];
+    float o[CPL], sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+        o[i] = __fmul_rn(O[0][i], inv1) - __fmul_rn(O[1][i], inv2);   // no contraction: exact cancel
+        sum += o[i];
+    }
+    const float mu = warp_sum(sum) * (1.0f / DV);
+    float sq = 0.f;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) sq += (o[i] - mu) * (o[i] - mu);
+    const float var = warp_sum(sq) * (1.0f / DV);
+    const float sc = (1.0f - p.lambda_init) * rsqrtf(var + p.eps);
+    const int col0 = lane * CPL;
+    if (p.o_prenorm) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) p.o_prenorm[bh * DV + col0 + i] = o[i];
+    }
+    uint32_t packed[CPL / 2];
+#pragma unroll
+    for (int i = 0; i < CPL / 2; ++i) {
+        const float g0 = p.gamma ? p.gamma[(size_t)h * DV + col0 + 2 * i] : 1.0f;
+        const float g1 = p.gamma ? p.gamma[(size_t)h * DV + col0 + 2 * i + 1] : 1.0f;
+        packed[i] = pack_bf16x2((o[2 * i] - mu) * sc * g0, (o[2 * i + 1] - mu) * sc * g1);
+    }
+    if constexpr (CPL == 4) {
+        *reinterpret_cast<uint2*>(p.out + bh * DV + col0) = make_uint2(packed[0], packed[1]);
+    } else {
+        *reinterpret_cast<uint32_t*>(p.out + bh * DV + col0) = packed[0];
+    }
+}
+
+}  // namespace diffattn

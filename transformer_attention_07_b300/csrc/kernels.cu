@@ -1,0 +1,172 @@
+// Device code of the library and the host launchers that configure it.
+// Everything that runs on the GPU is in this translation unit, so the device
+// error word is a single object per device.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "launch.h"
+#include "sm103_ptx.cuh"
+
+namespace diffattn {
+
+__device__ int g_device_error = 0;
+
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int site) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*reinterpret_cast<volatile int*>(&g_device_error) != 0) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                atomicCAS(&g_device_error, 0, site);
+                return false;
+            }
+        }
+    }
+}
+
+}  // namespace diffattn
+
+#include "decode_sm103a.cuh"
+#include "prefill_sm103a.cuh"
+
+namespace diffattn {
+
+// ----------------------------------------------------------------- tensor maps
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 4-D bf16 map over a BHND tensor [B][H][N][W]: dims (W, N, H, B).
+static bool make_map_bhnd(CUtensorMap* m, const void* base, int B, int H, int N, int W, int box_w, int box_n,
+                          CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)W * 2, (cuuint64_t)N * W * 2, (cuuint64_t)H * N * W * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)box_w, (cuuint32_t)box_n, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ----------------------------------------------------------------- prefill
+
+template <int D, int DV, bool CAUSAL>
+static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
+    using L = PrefillLayout<D, DV>;
+    CUtensorMap mq1, mq2, mk1, mk2, mv;
+    const CUtensorMapSwizzle qk_swz = D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map_bhnd(&mq1, a.q1, a.B, a.H, a.Nq, D, D, L::BM, qk_swz) ||
+        !make_map_bhnd(&mq2, a.q2, a.B, a.H, a.Nq, D, D, L::BM, qk_swz) ||
+        !make_map_bhnd(&mk1, a.k1, a.B, a.H, a.Nk, D, D, L::BN, qk_swz) ||
+        !make_map_bhnd(&mk2, a.k2, a.B, a.H, a.Nk, D, D, L::BN, qk_swz) ||
+        !make_map_bhnd(&mv, a.v, a.B, a.H, a.Nk, DV, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return LAUNCH_ERR_CUDA;
+    PrefillParams p;
+    p.B = a.B;
+    p.H = a.H;
+    p.Nq = a.Nq;
+    p.Nk = a.Nk;
+    p.lambda = a.lambda;
+    p.lambda_init = a.lambda_init;
+    p.eps = a.eps;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    p.gamma = a.gamma;
+    p.out = static_cast<uint16_t*>(a.out);
+    p.o_prenorm = a.o_prenorm;
+    auto kern = prefill_kernel<D, DV, CAUSAL>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES) != cudaSuccess)
+        return LAUNCH_ERR_CUDA;
+    const dim3 grid((a.Nq + L::BM - 1) / L::BM, a.H, a.B);
+    kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq1, mq2, mk1, mk2, mv, p);
+    return cudaGetLastError() == cudaSuccess ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+}
+
+int launch_prefill(const PrefillArgs& a, cudaStream_t st) {
+    if (a.d == 64 && a.dv == 128)
+        return a.causal ? launch_prefill_t<64, 128, true>(a, st) : launch_prefill_t<64, 128, false>(a, st);
+    if (a.d == 32 && a.dv == 64)
+        return a.causal ? launch_prefill_t<32, 64, true>(a, st) : launch_prefill_t<32, 64, false>(a, st);
+    return LAUNCH_ERR_UNSUPPORTED;
+}
+
+// ----------------------------------------------------------------- decode
+
+template <int D, int DV>
+static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
+    using L = DecodeLayout<D, DV>;
+    // K1/K2 viewed as [B*H*Nk rows, D]: 32-row boxes with the swizzle that
+    // matches the row width.
+    CUtensorMap mk1, mk2;
+    const CUtensorMapSwizzle swz = D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const int rows = a.B * a.H * a.Nk;
+    if (!make_map_bhnd(&mk1, a.k1, 1, 1, rows, D, D, L::KC, swz) ||
+        !make_map_bhnd(&mk2, a.k2, 1, 1, rows, D, D, L::KC, swz))
+        return LAUNCH_ERR_CUDA;
+    DecodeParams p;
+    p.q1 = static_cast<const uint16_t*>(a.q1);
+    p.q2 = static_cast<const uint16_t*>(a.q2);
+    p.v = static_cast<const uint16_t*>(a.v);
+    p.B = a.B;
+    p.H = a.H;
+    p.Nk = a.Nk;
+    p.S = a.splits;
+    p.keys_per_split = a.keys_per_split;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    p.ws = a.ws;
+    auto kern = decode_split_kernel<D, DV>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES) != cudaSuccess)
+        return LAUNCH_ERR_CUDA;
+    kern<<<dim3(a.splits, a.H, a.B), L::THREADS, L::SMEM_BYTES, st>>>(mk1, mk2, p);
+    if (cudaGetLastError() != cudaSuccess) return LAUNCH_ERR_CUDA;
+    MergeParams mp;
+    mp.B = a.B;
+    mp.H = a.H;
+    mp.S = a.splits;
+    mp.lambda = a.lambda;
+    mp.lambda_init = a.lambda_init;
+    mp.eps = a.eps;
+    mp.ws = a.ws;
+    mp.gamma = a.gamma;
+    mp.out = static_cast<uint16_t*>(a.out);
+    mp.o_prenorm = a.o_prenorm;
+    const int heads = a.B * a.H;
+    decode_merge_kernel<DV><<<(heads + 3) / 4, 128, 0, st>>>(mp);
+    return cudaGetLastError() == cudaSuccess ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+}
+
+int launch_decode(const DecodeArgs& a, cudaStream_t st) {
+    if (a.d == 64 && a.dv == 128) return launch_decode_t<64, 128>(a, st);
+    if (a.d == 32 && a.dv == 64) return launch_decode_t<32, 64>(a, st);
+    return LAUNCH_ERR_UNSUPPORTED;
+}
+
+int read_and_clear_device_error(cudaStream_t st, int* value) {
+    if (cudaStreamSynchronize(st) != cudaSuccess) return LAUNCH_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return LAUNCH_ERR_CUDA;
+    const int zero = 0;
+    if (v != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return LAUNCH_ERR_CUDA;
+    *value = v;
+    return LAUNCH_OK;
+}
+
+}  // namespace diffattn

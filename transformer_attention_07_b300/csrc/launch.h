@@ -1,0 +1,37 @@
+// Internal interface between the C ABI (argument checking) and the launchers
+// (tensor maps, grids, kernels).  Not installed; the public header is
+// include/diffattn.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace diffattn {
+
+enum LaunchStatus { LAUNCH_OK = 0, LAUNCH_ERR_CUDA = 1, LAUNCH_ERR_UNSUPPORTED = 2 };
+
+struct PrefillArgs {
+    const void *q1, *k1, *q2, *k2, *v;
+    float lambda, lambda_init, eps;
+    int causal, B, H, Nq, Nk, d, dv;
+    const float* gamma;
+    void* out;
+    float* o_prenorm;
+};
+
+struct DecodeArgs {
+    const void *q1, *k1, *q2, *k2, *v;
+    float lambda, lambda_init, eps;
+    int B, H, Nk, d, dv;
+    int splits, keys_per_split;
+    const float* gamma;
+    float* ws;
+    void* out;
+    float* o_prenorm;
+};
+
+int launch_prefill(const PrefillArgs& a, cudaStream_t st);
+int launch_decode(const DecodeArgs& a, cudaStream_t st);
+int read_and_clear_device_error(cudaStream_t st, int* value);
+
+}  // namespace diffattn

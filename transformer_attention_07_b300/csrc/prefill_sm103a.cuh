@@ -1,0 +1,384 @@
+// Fused differential-attention prefill for sm_103a.
+//
+// Computes, per head and per query row i (Differential Transformer pages:
+// the DiffAttn formula of the iloveeagents.com Q&A, "Mathematical Formula";
+// steps 2-4 of llmbytes.dev "How Differential Attention Cancels Common-Mode
+// Noise"):
+//     o_i = sum_j (A1_ij - lambda A2_ij) v_j
+//     y_i = (1 - lambda_init) * gamma * (o_i - mean(o_i)) / sqrt(var(o_i) + eps)
+// without ever forming an N x N map.  Because the product with V is linear,
+// (A1 - lambda A2) V = A1 V - lambda A2 V, so each map keeps its own online
+// softmax state (running max m_r, normaliser l_r) and its own unnormalised
+// accumulator O_r, and the two are combined once per row at the end:
+//     o = O1 / l1 - lambda * O2 / l2.
+//
+// One CTA owns a tile of 128 query rows of one (b, h) and walks the key tiles
+// (128 keys each; under causal masking only the tiles at or left of the
+// diagonal).  Warp roles:
+//   warp 0       TMA producer: Q1/Q2 once, then K1/K2 and V tiles into
+//                shared-memory rings (128-byte swizzle).
+//   warp 1       tensor-core issuer (one thread) and TMEM owner:
+//                  S_r = Q_r K_r^T           (tcgen05.mma, A and B in smem)
+//                  O_r += P_r V              (tcgen05.mma, A = P in TMEM)
+//   warps 4-7    softmax of map 1; warps 8-11 softmax of map 2.  Thread t of
+//                the group owns query row t: it reads its row of S_r from
+//                TMEM, updates (m_r, l_r), writes P_r (bf16) back over S_r,
+//                and rescales O_r in TMEM when its max has grown by more than
+//                2^8 (values stay bounded by 2^8 in between).
+//   epilogue     both softmax groups: o = O1/l1 - lambda O2/l2 per row, the
+//                GroupNorm statistics over dv, gain, (1 - lambda_init), bf16
+//                store (and the optional fp32 pre-norm copy).
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   [0,128) S1 (P1 aliases its first 64 columns)   [128,256) S2 / P2
+//   [256,256+dv) O1                                [256+dv,256+2dv) O2
+#pragma once
+
+#include "sm103_ptx.cuh"
+
+namespace diffattn {
+
+struct PrefillParams {
+    int B, H, Nq, Nk;
+    float lambda, lambda_init, eps;
+    float scale_log2;       // log2(e) / sqrt(d)
+    const float* gamma;     // [H*dv] or null
+    uint16_t* out;          // bf16 [B,H,Nq,dv]
+    float* o_prenorm;       // fp32 [B,H,Nq,dv] or null
+};
+
+template <int D, int DV>
+struct PrefillLayout {
+    static constexpr int BM = 128;   // query rows per tile (MMA M)
+    static constexpr int BN = 128;   // keys per tile (MMA N of QK^T, K of PV)
+    static constexpr int KST = 3;    // K1/K2 ring depth
+    static constexpr int VST = 2;    // V ring depth
+    static constexpr uint32_t Q_BYTES = BM * D * 2;
+    static constexpr uint32_t K_BYTES = BN * D * 2;
+    static constexpr uint32_t V_BOX = BN * 128;   // one 64-column V box: BN rows x 128 bytes
+    static constexpr uint32_t V_BYTES = BN * DV * 2;
+    static constexpr uint32_t OFF_Q1 = 0;
+    static constexpr uint32_t OFF_Q2 = Q_BYTES;
+    static constexpr uint32_t OFF_K = 2 * Q_BYTES;              // stage s: K1 then K2
+    static constexpr uint32_t OFF_V = OFF_K + KST * 2 * K_BYTES;
+    static constexpr uint32_t OFF_EPI = OFF_V + VST * V_BYTES;  // 6 x 128 fp32 exchange slots
+    static constexpr uint32_t OFF_BAR = OFF_EPI + 6 * BM * 4;
+    // barrier indices
+    static constexpr int B_Q = 0;
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_KEMPTY = B_KFULL + KST;
+    static constexpr int B_VFULL = B_KEMPTY + KST;
+    static constexpr int B_VEMPTY = B_VFULL + VST;
+    static constexpr int B_SFULL = B_VEMPTY + VST;   // 2 (one per map)
+    static constexpr int B_PFULL = B_SFULL + 2;      // 2
+    static constexpr int B_OFULL = B_PFULL + 2;
+    static constexpr int NBAR = B_OFULL + 1;
+    static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
+    // +1024 for aligning the dynamic base; at least 120 KB so that a single
+    // CTA (which takes all 512 TMEM columns) is resident per SM.
+    static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u) ? USED + 1024 : 120u * 1024u;
+    static constexpr uint32_t QK_SWZ = (D == 64) ? SWZ_128B : SWZ_64B;
+    static constexpr uint32_t QK_SBO = 8 * D * 2;    // bytes between 8-row groups
+    static constexpr uint32_t TM_S1 = 0, TM_S2 = 128, TM_O1 = 256, TM_O2 = 256 + DV;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int THREADS = 384;
+    static_assert(D == 64 || D == 32, "d");
+    static_assert(DV == 128 || DV == 64, "dv");
+    static_assert(USED + 1024 <= 227u * 1024u, "shared memory");
+};
+
+template <int D, int DV, bool CAUSAL>
+__global__ void __launch_bounds__(384, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
+               const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
+               const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+    using L = PrefillLayout<D, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    // Tile: heaviest (right-most under causal masking) query tiles first.
+    const int num_qt = (p.Nq + L::BM - 1) / L::BM;
+    const int qt = num_qt - 1 - (int)blockIdx.x;
+    const int h = blockIdx.y, b = blockIdx.z;
+    const int q0 = qt * L::BM;
+    const int diag = p.Nk - p.Nq;   // key j visible to query i iff j <= i + diag (causal)
+    int kv_end = p.Nk;
+    if (CAUSAL) kv_end = min(p.Nk, q0 + L::BM + diag);
+    const int n_kv = (kv_end + L::BN - 1) / L::BN;
+
+    auto bar = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)i; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::B_Q), 1);
+        for (int s = 0; s < L::KST; ++s) {
+            mbar_init(bar(L::B_KFULL + s), 1);
+            mbar_init(bar(L::B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < L::VST; ++s) {
+            mbar_init(bar(L::B_VFULL + s), 1);
+            mbar_init(bar(L::B_VEMPTY + s), 1);
+        }
+        for (int r = 0; r < 2; ++r) {
+            mbar_init(bar(L::B_SFULL + r), 1);
+            mbar_init(bar(L::B_PFULL + r), 128);
+        }
+        mbar_init(bar(L::B_OFULL), 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_q1);
+        prefetch_tensormap(&tm_q2);
+        prefetch_tensormap(&tm_k1);
+        prefetch_tensormap(&tm_k2);
+        prefetch_tensormap(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(sb + L::OFF_TMEM_SLOT, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_TMEM_SLOT);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::Q_BYTES);
+            tma_load_4d(sb + L::OFF_Q1, &tm_q1, bar(L::B_Q), 0, q0, h, b);
+            tma_load_4d(sb + L::OFF_Q2, &tm_q2, bar(L::B_Q), 0, q0, h, b);
+            int k_issued = 0, v_issued = 0;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int ks = j % L::KST;
+                ok = mbar_wait(bar(L::B_KEMPTY + ks), ((j / L::KST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
+                if (!ok) break;
+                const uint32_t k1s = sb + L::OFF_K + (uint32_t)ks * 2 * L::K_BYTES;
+                mbar_arrive_expect_tx(bar(L::B_KFULL + ks), 2 * L::K_BYTES);
+                tma_load_4d(k1s, &tm_k1, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
+                tma_load_4d(k1s + L::K_BYTES, &tm_k2, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
+                ++k_issued;
+                const int vs = j % L::VST;
+                ok = mbar_wait(bar(L::B_VEMPTY + vs), ((j / L::VST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
+                if (!ok) break;
+                const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
+                mbar_arrive_expect_tx(bar(L::B_VFULL + vs), L::V_BYTES);
+#pragma unroll
+                for (int c = 0; c < DV / 64; ++c)
+                    tma_load_4d(vsm + (uint32_t)c * L::V_BOX, &tm_v, bar(L::B_VFULL + vs), c * 64, j * L::BN, h, b);
+                ++v_issued;
+            }
+            // Never leave with copies in flight: wait (bounded) for the last
+            // phase armed on every stage.
+            mbar_wait(bar(L::B_Q), 0, ERR_SITE_PREFILL_DRAIN);
+            for (int s = 0; s < L::KST && s < k_issued; ++s) {
+                const int last = s + ((k_issued - 1 - s) / L::KST) * L::KST;
+                mbar_wait(bar(L::B_KFULL + s), (last / L::KST) & 1, ERR_SITE_PREFILL_DRAIN);
+            }
+            for (int s = 0; s < L::VST && s < v_issued; ++s) {
+                const int last = s + ((v_issued - 1 - s) / L::VST) * L::VST;
+                mbar_wait(bar(L::B_VFULL + s), (last / L::VST) & 1, ERR_SITE_PREFILL_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(L::BM, L::BN, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(L::BM, DV, true);
+            bool ok = mbar_wait(bar(L::B_Q), 0, ERR_SITE_PREFILL_MMA);
+            tc_fence_after();
+            const uint64_t dq[2] = {smem_desc(sb + L::OFF_Q1, 16, L::QK_SBO, L::QK_SWZ),
+                                    smem_desc(sb + L::OFF_Q2, 16, L::QK_SBO, L::QK_SWZ)};
+            const uint32_t s_col[2] = {L::TM_S1, L::TM_S2};
+            const uint32_t o_col[2] = {L::TM_O1, L::TM_O2};
+            for (int j = 0; j <= n_kv && ok; ++j) {
+                const int ks = j % L::KST;
+                if (j < n_kv) {
+                    ok = mbar_wait(bar(L::B_KFULL + ks), (j / L::KST) & 1, ERR_SITE_PREFILL_MMA);
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                const int jv = j - 1;
+                const int vs = (jv + L::VST) % L::VST;
+                if (jv >= 0) {
+                    ok = mbar_wait(bar(L::B_VFULL + vs), (jv / L::VST) & 1, ERR_SITE_PREFILL_MMA);
+                    if (!ok) break;
+                }
+                const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
+                const uint32_t k_base = sb + L::OFF_K + (uint32_t)ks * 2 * L::K_BYTES;
+                for (int r = 0; r < 2; ++r) {
+                    // O_r += P_r V for the previous key tile (P_r sits over S_r).
+                    if (jv >= 0) {
+                        ok = mbar_wait(bar(L::B_PFULL + r), jv & 1, ERR_SITE_PREFILL_MMA);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < L::BN / 16; ++k) {
+                            const uint64_t bdesc = smem_desc(vsm + (uint32_t)k * 16 * 128, L::V_BOX, 1024, SWZ_128B);
+                            mma_ts(tmem + o_col[r], tmem + s_col[r] + (uint32_t)k * 8, bdesc, idesc_pv,
+                                   (jv > 0 || k > 0) ? 1u : 0u);
+                        }
+                        if (r == 1) mma_commit(bar(L::B_VEMPTY + vs));
+                    }
+                    // S_r = Q_r K_r^T for this key tile.
+                    if (j < n_kv) {
+                        const uint32_t kr = k_base + (uint32_t)r * L::K_BYTES;
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint64_t bdesc = smem_desc(kr + (uint32_t)k * 32, 16, L::QK_SBO, L::QK_SWZ);
+                            mma_ss(tmem + s_col[r], dq[r] + (uint64_t)(k * 2), bdesc, idesc_qk, k > 0 ? 1u : 0u);
+                        }
+                        mma_commit(bar(L::B_SFULL + r));
+                        if (r == 1) mma_commit(bar(L::B_KEMPTY + ks));
+                    }
+                }
+            }
+            // Always signal the epilogue (also after a failed wait) once every
+            // MMA issued so far has completed.
+            mma_commit(bar(L::B_OFULL));
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax
+        const int r = (warp - 4) >> 2;           // map
+        const int wq = warp & 3;                 // TMEM lane quarter of this warp
+        const int row = wq * 32 + lane;          // row within the tile
+        const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+        const uint32_t s_col = r ? L::TM_S2 : L::TM_S1;
+        const uint32_t o_col = r ? L::TM_O2 : L::TM_O1;
+        const int qi = q0 + row;
+        const int kmax = CAUSAL ? min(qi + diag, p.Nk - 1) : p.Nk - 1;   // last visible key
+        const float sl2 = p.scale_log2;
+        float m = -INFINITY;   // running max of scaled logits (log2 domain)
+        float l = 0.f;         // running sum of the bf16-rounded probabilities
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            ok = mbar_wait(bar(L::B_SFULL + r), j & 1, ERR_SITE_PREFILL_SOFTMAX);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sv[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + t_lane + s_col + 32u * c, sv[c]);
+            const int kb = j * L::BN;
+            if (kb + L::BN - 1 > kmax) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (kb + 32 * c + i > kmax) sv[c][i] = __float_as_uint(-INFINITY);
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
+            const float m_new = fmaxf(m, mx * sl2);
+            const bool grow = m_new > m + 8.0f;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float alpha = grow ? fast_exp2(m - m_new) : 1.0f;
+                if (j > 0) {
+                    // O_r *= alpha (the previous P_r V has completed: it was
+                    // issued before this tile's S_r, whose commit we waited on).
+#pragma unroll
+                    for (int c = 0; c < DV / 32; ++c) {
+                        uint32_t ov[32];
+                        tmem_ld32(tmem + t_lane + o_col + 32u * c, ov);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                        tmem_st32(tmem + t_lane + o_col + 32u * c, ov);
+                    }
+                }
+                if (grow) {
+                    l *= alpha;
+                    m = m_new;
+                }
+            }
+            const float mb = (m == -INFINITY) ? 0.f : m;
+            uint32_t pk[2][32];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * i]), sl2, -mb));
+                    const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, -mb));
+                    const uint32_t w = pack_bf16x2(p0, p1);
+                    pk[c >> 1][(c & 1) * 16 + i] = w;
+                    lsum += bf16lo_to_f32(w) + bf16hi_to_f32(w);
+                }
+            l += lsum;
+            tmem_st32(tmem + t_lane + s_col, pk[0]);
+            tmem_st32(tmem + t_lane + s_col + 32u, pk[1]);
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(L::B_PFULL + r));
+        }
+
+        // ------------------------------------------------------------ epilogue
+        mbar_wait(bar(L::B_OFULL), 0, ERR_SITE_PREFILL_EPILOGUE);
+        __syncwarp();
+        tc_fence_after();
+        float* epi = reinterpret_cast<float*>(smem + L::OFF_EPI);
+        epi[r * L::BM + row] = l;
+        named_barrier_sync(1, 256);
+        const float inv1 = 1.0f / epi[row];
+        const float inv2 = p.lambda / epi[L::BM + row];
+        constexpr int HALF = DV / 2;
+        const int c0 = r * HALF;
+        float o[HALF];
+#pragma unroll
+        for (int c = 0; c < HALF / 32; ++c) {
+            uint32_t a[32], bb[32];
+            tmem_ld32(tmem + t_lane + L::TM_O1 + c0 + 32u * c, a);
+            tmem_ld32(tmem + t_lane + L::TM_O2 + c0 + 32u * c, bb);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                // Both products rounded before the subtraction (no FMA
+                // contraction), so identical maps with lambda = 1 cancel to 0.
+                o[32 * c + i] = __fmul_rn(__uint_as_float(a[i]), inv1) - __fmul_rn(__uint_as_float(bb[i]), inv2);
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < HALF; ++i) sum += o[i];
+        epi[(2 + r) * L::BM + row] = sum;
+        named_barrier_sync(1, 256);
+        const float mu = (epi[2 * L::BM + row] + epi[3 * L::BM + row]) * (1.0f / DV);
+        float sq = 0.f;
+#pragma unroll
+        for (int i = 0; i < HALF; ++i) sq += (o[i] - mu) * (o[i] - mu);
+        epi[(4 + r) * L::BM + row] = sq;
+        named_barrier_sync(1, 256);
+        const float var = (epi[4 * L::BM + row] + epi[5 * L::BM + row]) * (1.0f / DV);
+        const float sc = (1.0f - p.lambda_init) * rsqrtf(var + p.eps);
+        if (qi < p.Nq) {
+            const size_t rowoff = (((size_t)b * p.H + h) * p.Nq + qi) * DV + c0;
+            if (p.o_prenorm) {
+                float4* dst = reinterpret_cast<float4*>(p.o_prenorm + rowoff);
+#pragma unroll
+                for (int i = 0; i < HALF / 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
+            const float* g = p.gamma ? p.gamma + (size_t)h * DV + c0 : nullptr;
+            uint4* dst = reinterpret_cast<uint4*>(p.out + rowoff);
+#pragma unroll
+            for (int i = 0; i < HALF / 8; ++i) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = (o[8 * i + e] - mu) * sc * (g ? g[8 * i + e] : 1.0f);
+                dst[i] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                                    pack_bf16x2(y[6], y[7]));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+}  // namespace diffattn

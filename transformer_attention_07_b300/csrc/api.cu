@@ -114,8 +114,10 @@ int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* 
     int splits = num_splits;
     if (splits == 0) {
         int dev = 0, sms = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        if (!diffattn::cuda_ok(cudaGetDevice(&dev), "decode: get device") ||
+            !diffattn::cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                               "decode: SM count") ||
+            sms < 1)
             return DIFFATTN_ERR_CUDA;
         splits = choose_splits((int64_t)B * H, Nk, sms);
     }

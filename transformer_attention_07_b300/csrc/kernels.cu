@@ -7,6 +7,8 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "launch.h"
@@ -37,6 +39,15 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int s
 
 namespace diffattn {
 
+// ----------------------------------------------------------------- diagnostics
+
+bool cuda_ok(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return true;
+    static const bool debug = std::getenv("DIFFATTN_DEBUG") != nullptr;
+    if (debug) std::fprintf(stderr, "[diffattn] %s failed: %s (%d)\n", what, cudaGetErrorString(e), (int)e);
+    return false;
+}
+
 // ----------------------------------------------------------------- tensor maps
 
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -62,9 +73,12 @@ static bool make_map_bhnd(CUtensorMap* m, const void* base, int B, int H, int N,
     const cuuint64_t strides[3] = {(cuuint64_t)W * 2, (cuuint64_t)N * W * 2, (cuuint64_t)H * N * W * 2};
     const cuuint32_t box[4] = {(cuuint32_t)box_w, (cuuint32_t)box_n, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS && std::getenv("DIFFATTN_DEBUG"))
+        std::fprintf(stderr, "[diffattn] cuTensorMapEncodeTiled failed: %d\n", (int)r);
+    return r == CUDA_SUCCESS;
 }
 
 // ----------------------------------------------------------------- prefill
@@ -93,11 +107,12 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     p.out = static_cast<uint16_t*>(a.out);
     p.o_prenorm = a.o_prenorm;
     auto kern = prefill_kernel<D, DV, CAUSAL>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES) != cudaSuccess)
+    if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
+                 "prefill: set shared memory"))
         return LAUNCH_ERR_CUDA;
     const dim3 grid((a.Nq + L::BM - 1) / L::BM, a.H, a.B);
     kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq1, mq2, mk1, mk2, mv, p);
-    return cudaGetLastError() == cudaSuccess ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+    return cuda_ok(cudaGetLastError(), "prefill: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }
 
 int launch_prefill(const PrefillArgs& a, cudaStream_t st) {
@@ -133,10 +148,11 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     p.ws = a.ws;
     auto kern = decode_split_kernel<D, DV>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES) != cudaSuccess)
+    if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
+                 "decode: set shared memory"))
         return LAUNCH_ERR_CUDA;
     kern<<<dim3(a.splits, a.H, a.B), L::THREADS, L::SMEM_BYTES, st>>>(mk1, mk2, p);
-    if (cudaGetLastError() != cudaSuccess) return LAUNCH_ERR_CUDA;
+    if (!cuda_ok(cudaGetLastError(), "decode: split launch")) return LAUNCH_ERR_CUDA;
     MergeParams mp;
     mp.B = a.B;
     mp.H = a.H;
@@ -150,7 +166,7 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     mp.o_prenorm = a.o_prenorm;
     const int heads = a.B * a.H;
     decode_merge_kernel<DV><<<(heads + 3) / 4, 128, 0, st>>>(mp);
-    return cudaGetLastError() == cudaSuccess ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+    return cuda_ok(cudaGetLastError(), "decode: merge launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t st) {

@@ -30,6 +30,10 @@ struct DecodeArgs {
     float* o_prenorm;
 };
 
+// With DIFFATTN_DEBUG set in the environment, a failing CUDA call is
+// reported on stderr (call site and the runtime's error string).
+bool cuda_ok(cudaError_t e, const char* what);
+
 int launch_prefill(const PrefillArgs& a, cudaStream_t st);
 int launch_decode(const DecodeArgs& a, cudaStream_t st);
 int read_and_clear_device_error(cudaStream_t st, int* value);

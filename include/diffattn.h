@@ -109,6 +109,43 @@ int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* 
                     void* workspace, size_t workspace_bytes,
                     void* out, float* o_prenorm, void* stream);
 
+/*
+ * Split-KV decode that allocates nothing: the same computation and arguments
+ * as diffattn_decode, minus the workspace.  (The Differential Transformer
+ * pages have no counterpart to this entry point; it exists for callers.)
+ *
+ * Who needs it: callers that cannot call cudaMalloc at the point of use —
+ * for example a plugin or operator inside a serving framework that owns all
+ * device memory through a pool planned ahead of time and forbids allocation
+ * on the request path, or an interface that hands the operator only its
+ * input and output pointers and no allocator.
+ *
+ * Scratch: the per-split partial softmax states go to one library-owned
+ * device array of 8 MiB (8388608 bytes), a file-scope static that every GPU
+ * which loads the library holds until the process exits.  A problem needs
+ * B*H*splits*2*(dv + 4)*4 bytes of it (splits as chosen for num_splits = 0,
+ * or as given); a problem that needs more is rejected with
+ * DIFFATTN_ERR_WORKSPACE and nothing is launched.  No call allocates or frees
+ * device memory (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * array's device address once (cudaGetSymbolAddress) and caches it; make
+ * that first call before any stream capture.
+ *
+ * Sharing: every call uses the same array and it keeps the last call's
+ * contents.  Nothing in it needs to start at zero: each call writes every
+ * partial before reading it.  Calls whose kernels overlap on the GPU (two
+ * streams, or two host threads) race on the array and corrupt each other's
+ * results; serialise them.
+ *
+ * Returns the same statuses as diffattn_decode; DIFFATTN_ERR_CUDA also when
+ * the scratch address cannot be obtained.
+ */
+int diffattn_decode_noalloc(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                            float lambda, float lambda_init, int B, int H, int Nk, int d, int dv,
+                            const float* gn_gamma, float eps, int num_splits,
+                            void* out, float* o_prenorm, void* stream);
+
 /* Static description of a status code. */
 const char* diffattn_status_string(int status);
 

@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "diffattn_fwd", "diffattn_fwd_ex", "diffattn_decode_workspace_bytes", "diffattn_decode",
-        "diffattn_status_string", "diffattn_last_device_error"])
+        "diffattn_decode_noalloc", "diffattn_status_string", "diffattn_last_device_error"])
 
 
 def test_library_exports_every_declared_symbol(lib):

@@ -130,6 +130,21 @@ int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* 
     return from_launch(diffattn::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+// Decode for callers that cannot allocate device memory: the split partials
+// go to the library's own static scratch instead of a caller workspace.  All
+// argument checks are those of diffattn_decode; a problem whose partials do
+// not fit the scratch is rejected there with DIFFATTN_ERR_WORKSPACE.
+int diffattn_decode_noalloc(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                            float lambda, float lambda_init, int B, int H, int Nk, int d, int dv,
+                            const float* gn_gamma, float eps, int num_splits, void* out, float* o_prenorm,
+                            void* stream) {
+    void* scratch = nullptr;
+    size_t scratch_bytes = 0;
+    if (diffattn::decode_noalloc_scratch(&scratch, &scratch_bytes) != diffattn::LAUNCH_OK) return DIFFATTN_ERR_CUDA;
+    return diffattn_decode(q1, k1, q2, k2, v, lambda, lambda_init, B, H, Nk, d, dv, gn_gamma, eps, num_splits,
+                           scratch, scratch_bytes, out, o_prenorm, stream);
+}
+
 const char* diffattn_status_string(int status) {
     switch (status) {
         case DIFFATTN_OK: return "ok";

@@ -175,6 +175,35 @@ int launch_decode(const DecodeArgs& a, cudaStream_t st) {
     return LAUNCH_ERR_UNSUPPORTED;
 }
 
+// ----------------------------------------------------------------- decode without allocation
+//
+// Scratch for diffattn_decode_noalloc: the split partials live in this
+// file-scope device array instead of a caller-provided workspace.  Every
+// device that loads the library holds these 8 MiB until the process exits.
+// In host code the array's name is only a stand-in, so its device address is
+// looked up with cudaGetSymbolAddress, once per device, with that device
+// current, and cached.
+static __device__ __align__(256) float g_decode_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+int decode_noalloc_scratch(void** ptr, size_t* bytes) {
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = -1;
+    if (!cuda_ok(cudaGetDevice(&dev), "no-alloc decode: get device") || dev < 0 || dev >= kMaxDevices)
+        return LAUNCH_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (!cuda_ok(cudaGetSymbolAddress(&p, g_decode_scratch), "no-alloc decode: scratch address") || !p)
+            return LAUNCH_ERR_CUDA;
+        addr[dev] = p;
+    }
+    *ptr = addr[dev];
+    *bytes = kNoAllocScratchBytes;
+    return LAUNCH_OK;
+}
+
 int read_and_clear_device_error(cudaStream_t st, int* value) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return LAUNCH_ERR_CUDA;
     int v = 0;

@@ -38,4 +38,11 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t st);
 int launch_decode(const DecodeArgs& a, cudaStream_t st);
 int read_and_clear_device_error(cudaStream_t st, int* value);
 
+// Capacity of the library-owned decode scratch (diffattn_decode_noalloc).
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+
+// Device address and size of that scratch on the current device (looked up
+// on the first call per device).
+int decode_noalloc_scratch(void** ptr, size_t* bytes);
+
 }  // namespace diffattn

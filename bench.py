@@ -119,6 +119,23 @@ def dist_setup():
     return world, rank, local
 
 
+def reduce_max_over_ranks(vals, world, device):
+    """Element-wise maximum of per-rank timings (the job is as slow as its
+    slowest rank); identity on one rank."""
+    if world == 1:
+        return list(vals)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(vals), device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws an independent problem of the same shape."""
+    return base_seed + 1000 * rank
+
+
 def oracle_sample(w, inp_cpu, rows):
     import oracle
     (o, y), dt = oracle.timed_fwd(*inp_cpu, w.lam, w.lam_init, causal=w.causal, eps=w.eps, rows=rows,
@@ -177,8 +194,8 @@ def run_cuda(args, world, rank, local):
     wp, wd = WORKLOADS[args.prefill_workload], WORKLOADS[args.decode_workload]
     do_pre, do_dec = args.only in ("all", "prefill"), args.only in ("all", "decode")
     # Each rank its own independent problem (seed offset by rank).
-    pin = make_inputs(wp, device=dev, seed=wp.seed + 1000 * rank) if do_pre else None
-    din = make_inputs(wd, device=dev, seed=wd.seed + 1000 * rank) if do_dec else None
+    pin = make_inputs(wp, device=dev, seed=rank_seed(wp.seed, rank)) if do_pre else None
+    din = make_inputs(wd, device=dev, seed=rank_seed(wd.seed, rank)) if do_dec else None
     pout = torch.empty((wp.B, wp.H, wp.Nq, wp.dv), dtype=torch.bfloat16, device=dev) if do_pre else None
     dout = torch.empty((wd.B, wd.H, 1, wd.dv), dtype=torch.bfloat16, device=dev) if do_dec else None
     ws = torch.empty(da.decode_workspace_bytes(wd.B, wd.H, wd.Nk, wd.dv, 0), dtype=torch.uint8,
@@ -201,12 +218,7 @@ def run_cuda(args, world, rank, local):
             dist.barrier()
 
     def max_over_ranks(vals):
-        if world == 1:
-            return vals
-        import torch.distributed as dist
-        t = torch.tensor(vals, device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return t.tolist()
+        return reduce_max_over_ranks(vals, world, dev)
 
     for _ in range(args.warmup):
         prefill()

@@ -1,0 +1,56 @@
+"""Host-side multi-rank logic of bench.py on CPU (gloo, world size 2): each
+rank draws an independent problem, and the timed result is the maximum over
+ranks.  No GPU and no data-path collective are involved."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mine = [10.0 + rank, 5.0 - rank, 7.0 * (rank + 1)]
+        got = bench.reduce_max_over_ranks(mine, world, torch.device("cpu"))
+        q.put((rank, got, bench.rank_seed(1003, rank)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_max_and_draw_distinct_problems():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, got, seed in results:
+        assert got == [11.0, 5.0, 14.0]
+    seeds = {seed for _, _, seed in results}
+    assert len(seeds) == world
+
+
+def test_single_rank_is_identity():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_max_over_ranks([1.0, 2.0], 1, None) == [1.0, 2.0]

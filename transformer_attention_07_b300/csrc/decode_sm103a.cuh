@@ -5,8 +5,9 @@
 // Pass 1 (decode_split_kernel), grid (splits, H, B): a CTA owns one key range
 // of one (b, h).  A producer warp streams 32-key chunks of K1 and K2 (tiled
 // TMA, 128/64-byte swizzle so that lane-per-key reads are conflict-free) and
-// of V (bulk copy) into a 12-16 stage shared-memory ring.  Eight consumer
-// warps take chunks round-robin; in a warp, lane t scores key t against q1
+// of V (bulk copy) into a 12-16 stage shared-memory ring.  Six (d = 64) or
+// eight (d = 32) consumer warps take chunks round-robin, each always from the
+// same stages of the ring; in a warp, lane t scores key t against q1
 // and q2, the warp keeps one online-softmax state per map (max m_r, per-lane
 // partial normaliser l_r, unnormalised output O_r spread over the lanes by dv
 // column) and accumulates O_r += p_r[j] v_j with the probabilities broadcast
@@ -49,12 +50,19 @@ struct MergeParams {
 template <int D, int DV>
 struct DecodeLayout {
     static constexpr int KC = 32;                       // keys per chunk (one per lane)
-    static constexpr int NCW = 8;                       // consumer warps
+    // Chunk c goes to stage c % NST and to consumer warp c % NCW.  NST is a
+    // multiple of NCW, so every stage is always consumed by the same warp,
+    // which takes that stage's phases in order.  (If another warp could own
+    // the next phase of a stage, it might wait on that stage's full barrier
+    // while the earlier phase is still incomplete; a parity wait cannot tell
+    // the two apart and would return at once.)
+    static constexpr int NCW = (D == 64) ? 6 : 8;       // consumer warps
     static constexpr int THREADS = (NCW + 1) * 32;      // + producer warp
     static constexpr uint32_t K_BYTES = KC * D * 2;
     static constexpr uint32_t V_BYTES = KC * DV * 2;
     static constexpr uint32_t STAGE = 2 * K_BYTES + V_BYTES;
     static constexpr int NST = (D == 64) ? 12 : 16;
+    static_assert(NST % NCW == 0, "each stage must belong to one consumer warp");
     static constexpr uint32_t OFF_RING = 0;
     static constexpr int PART = DV + 4;                 // floats per (map) partial
     static constexpr uint32_t OFF_RED = NST * STAGE;    // NCW x 2 x PART floats

@@ -259,23 +259,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint32_t sv[4][32];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tmem + t_lane + s_col + 32u * c, sv[c]);
+            // S_r row: 128 columns in one TMEM load.
+            uint32_t sv[128];
+            tmem_ld128(tmem + t_lane + s_col, sv);
             const int kb = j * L::BN;
             if (kb + L::BN - 1 > kmax) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (kb + 32 * c + i > kmax) sv[c][i] = __float_as_uint(-INFINITY);
+                for (int i = 0; i < 128; ++i)
+                    if (kb + i > kmax) sv[i] = __float_as_uint(-INFINITY);
             }
-            float mx = -INFINITY;
+            // Row max: four independent chains of three-input maxima.
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sv[c][i]));
-            const float m_new = fmaxf(m, mx * sl2);
+            for (int i = 0; i < 128; i += 8) {
+                mx0 = fmax3(mx0, __uint_as_float(sv[i + 0]), __uint_as_float(sv[i + 1]));
+                mx1 = fmax3(mx1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
+                mx2 = fmax3(mx2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
+                mx3 = fmax3(mx3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
+            }
+            const float m_new = fmaxf(m, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2);
             const bool grow = m_new > m + 8.0f;
             if (__any_sync(0xffffffffu, grow)) {
                 const float alpha = grow ? fast_exp2(m - m_new) : 1.0f;
@@ -296,22 +298,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                     m = m_new;
                 }
             }
-            const float mb = (m == -INFINITY) ? 0.f : m;
-            uint32_t pk[2][32];
-            float lsum = 0.f;
+            // p = 2^(s * log2(e)/sqrt(d) - m): scale and shift two columns per
+            // packed FMA, exponential on the SFU, round to bf16 in pairs.  The
+            // row sum accumulates the rounded values (the P the MMA multiplies),
+            // so a row dominated by one key keeps that key's rounding out of
+            // O/l; four packed chains.
+            const float nm = (m == -INFINITY) ? 0.f : -m;
+            uint32_t pk[64];
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, a4 = 0.f, a5 = 0.f, a6 = 0.f, a7 = 0.f;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
+            for (int i = 0; i < 128; i += 8) {
+                float x[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * i]), sl2, -mb));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c][2 * i + 1]), sl2, -mb));
-                    const uint32_t w = pack_bf16x2(p0, p1);
-                    pk[c >> 1][(c & 1) * 16 + i] = w;
-                    lsum += bf16lo_to_f32(w) + bf16hi_to_f32(w);
-                }
-            l += lsum;
-            tmem_st32(tmem + t_lane + s_col, pk[0]);
-            tmem_st32(tmem + t_lane + s_col + 32u, pk[1]);
+                for (int e = 0; e < 8; e += 2)
+                    fma2_bcast(x[e], x[e + 1], __uint_as_float(sv[i + e]), __uint_as_float(sv[i + e + 1]), sl2, nm);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = fast_exp2(x[e]);
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) pk[(i >> 1) + e] = w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                add2(a0, a1, a0, a1, bf16lo_to_f32(w[0]), bf16hi_to_f32(w[0]));
+                add2(a2, a3, a2, a3, bf16lo_to_f32(w[1]), bf16hi_to_f32(w[1]));
+                add2(a4, a5, a4, a5, bf16lo_to_f32(w[2]), bf16hi_to_f32(w[2]));
+                add2(a6, a7, a6, a7, bf16lo_to_f32(w[3]), bf16hi_to_f32(w[3]));
+            }
+            l += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
+            tmem_st64(tmem + t_lane + s_col, pk);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(L::B_PFULL + r));

@@ -317,10 +317,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 uint32_t w[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) pk[(i >> 1) + e] = w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
-                add2(a0, a1, a0, a1, bf16lo_to_f32(w[0]), bf16hi_to_f32(w[0]));
-                add2(a2, a3, a2, a3, bf16lo_to_f32(w[1]), bf16hi_to_f32(w[1]));
-                add2(a4, a5, a4, a5, bf16lo_to_f32(w[2]), bf16hi_to_f32(w[2]));
-                add2(a6, a7, a6, a7, bf16lo_to_f32(w[3]), bf16hi_to_f32(w[3]));
+                acc_bf16x2(a0, a1, w[0]);
+                acc_bf16x2(a2, a3, w[1]);
+                acc_bf16x2(a4, a5, w[2]);
+                acc_bf16x2(a6, a7, w[3]);
             }
             l += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
             tmem_st64(tmem + t_lane + s_col, pk);

@@ -240,6 +240,21 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[128]) {
         : "memory");
 }
 
+// 64 consecutive 32-bit columns of this thread's lane in one load, waited on.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31,"
+        " %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47,"
+        " %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63},"
+        " [%64];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : DA_R8(0), DA_R8(8), DA_R8(16), DA_R8(24), DA_R8(32), DA_R8(40), DA_R8(48), DA_R8(56)
+        : "r"(taddr)
+        : "memory");
+}
+
 // Store 64 consecutive 32-bit columns of this thread's lane (not waited on).
 __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64]) {
     asm volatile(
@@ -273,6 +288,17 @@ __device__ __forceinline__ void fma2_bcast(float& d0, float& d1, float a0, float
         "mov.b64 {%0, %1}, rd;\n\t}"
         : "=f"(d0), "=f"(d1)
         : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// acc_lo += low bf16 of w, acc_hi += high bf16 of w (fp32 accumulation of
+// bf16 inputs, no separate unpack).
+__device__ __forceinline__ void acc_bf16x2(float& acc_lo, float& acc_hi, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\t"
+        "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc_lo), "+f"(acc_hi)
+        : "r"(w));
 }
 
 __device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0, float b1) {

@@ -180,6 +180,51 @@ def run_reference(args, world, rank):
     return 0
 
 
+def compare_single_map(dev, reps=10):
+    """DiffAttn (d = 64 per map, dv = 128) against standard attention of the
+    same parameters (d = dv = 128), causal, at the 2K and 4K lengths the
+    pages quote a throughput overhead for (llmbytes.dev "Throughput and
+    Hardware Realities").  Attention kernels only, not a whole model."""
+    import torch
+    import transformer_attention_07_b300 as da
+    from transformer_attention_07_b300.workloads import COMPARE_SHAPES, WORKLOADS, make_inputs, standard_inputs
+    w = WORKLOADS["causal_2k"]
+    res = {}
+    stream = torch.cuda.current_stream(dev)
+    for B, H, N in COMPARE_SHAPES:
+        di = make_inputs(w, device=dev, B=B, H=H, Nq=N, Nk=N)
+        si = standard_inputs(B, H, N, device=dev)
+        dout = torch.empty((B, H, N, 128), dtype=torch.bfloat16, device=dev)
+        sout = torch.empty_like(dout)
+        runs = {
+            "diffattn": lambda: da.fwd(di["q1"], di["k1"], di["q2"], di["k2"], di["v"], w.lam, w.lam_init,
+                                       causal=True, gamma=di["gamma"], eps=w.eps, out=dout, stream=stream),
+            "standard": lambda: da.standard_fwd(si["q"], si["k"], si["v"], causal=True, out=sout, stream=stream),
+        }
+        ms = {}
+        for name, fn in runs.items():
+            for _ in range(3):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms[name] = e0.elapsed_time(e1) / reps
+        pairs = B * H * N * (N + 1) // 2
+        res[f"N{N}"] = {
+            "B": B, "H": H, "diffattn_ms": ms["diffattn"], "standard_ms": ms["standard"],
+            "diffattn_tflops": 4 * (64 + 128) * pairs / (ms["diffattn"] * 1e-3) / 1e12,
+            "standard_tflops": 4 * 128 * pairs / (ms["standard"] * 1e-3) / 1e12,
+            "throughput_change": ms["standard"] / ms["diffattn"] - 1.0,
+        }
+        del di, si, dout, sout
+    res["note"] = ("attention-kernel throughput of DiffAttn relative to standard attention at equal parameters; "
+                   "the pages' -9% (2K) and -10..-12% (4K) are whole-model tokens/s")
+    return res
+
+
 def run_cuda(args, world, rank, local):
     import torch
     import transformer_attention_07_b300 as da
@@ -319,6 +364,8 @@ def run_cuda(args, world, rank, local):
     line["gpu_launches"] = args.steps * ((1 if do_pre else 0) + (2 if do_dec else 0))
     line["clocks"] = clk.summary()
     line["wall_s_timed"] = wall
+    if args.only == "all" and not args.no_compare:
+        line["single_map_baseline"] = compare_single_map(dev)
     if do_pre and not args.no_cpu_baseline:
         cpu = [pin[k].cpu() for k in names]
         rows = sample_rows_uniform(wp.Nq, args.cpu_rows, 4242)
@@ -344,6 +391,8 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-compare", action="store_true",
+                    help="skip the DiffAttn vs single-map (standard attention) comparison")
     ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
                     help="run one stage per step (profiling of a single kernel)")
     ap.add_argument("--prefill-workload", default=PREFILL)

@@ -82,6 +82,23 @@ int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* 
                     const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream);
 
 /*
+ * Standard softmax attention, the single-map baseline the pages compare
+ * differential attention against ("Throughput and Hardware Realities",
+ * llmbytes.dev, against FlashAttention; the operator is the standard
+ * attention of the iloveeagents.com Q&A, "Detail"):
+ *     out = softmax(Q K^T / sqrt(d)) V        (no lambda, no GroupNorm)
+ *   q [B,H,Nq,d], k [B,H,Nk,d], v [B,H,Nk,dv] bf16, (d, dv) = (128, 128):
+ *   the width of one differential head's [q1; q2] and v, so that the two
+ *   operators are compared at equal parameters.
+ *   causal      0 or 1 (bottom-right aligned as above; Nq <= Nk)
+ *   out         [B,H,Nq,dv] bf16;  out_f32: NULL or [B,H,Nq,dv] fp32
+ * Same conventions and statuses as diffattn_fwd.
+ */
+int diffattn_standard_fwd(const void* q, const void* k, const void* v, int causal,
+                          int B, int H, int Nq, int Nk, int d, int dv,
+                          void* out, float* out_f32, void* stream);
+
+/*
  * Bytes of device workspace diffattn_decode needs for this shape and split
  * count (num_splits = 0: enough for any split count the library chooses).
  * Returns 0 for invalid sizes.

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "diffattn_fwd", "diffattn_fwd_ex", "diffattn_decode_workspace_bytes", "diffattn_decode",
-        "diffattn_decode_noalloc", "diffattn_status_string", "diffattn_last_device_error"])
+        "diffattn_decode_noalloc", "diffattn_standard_fwd", "diffattn_status_string",
+        "diffattn_last_device_error"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -74,6 +75,19 @@ def test_fwd_empty_problems_return_ok_without_launch(lib):
     assert fwd(lib, H=0) == OK
     assert fwd(lib, Nq=0) == OK
     assert fwd(lib, Nq=0, causal=1) == OK
+
+
+def test_standard_fwd_validation(lib):
+    std = lambda q=FAKE, causal=0, Nq=4, Nk=4, d=128, dv=128, out=FAKE, f32=None: lib.diffattn_standard_fwd(
+        q, q, q, causal, 1, 1, Nq, Nk, d, dv, out, f32, None)
+    assert std(q=None) == INVALID
+    assert std(out=None) == INVALID
+    assert std(Nk=0) == INVALID
+    assert std(causal=1, Nq=5, Nk=4) == INVALID
+    assert std(d=64, dv=128) == UNSUPPORTED
+    assert std(q=MISALIGNED) == INVALID
+    assert std(f32=MISALIGNED) == INVALID
+    assert std(Nq=0) == OK
 
 
 def test_decode_workspace_bytes(lib):

@@ -18,7 +18,7 @@ import ctypes
 import os
 
 __all__ = [
-    "fwd", "decode", "decode_workspace_bytes", "status_string", "last_device_error",
+    "fwd", "standard_fwd", "decode", "decode_workspace_bytes", "status_string", "last_device_error",
     "load", "LIB_PATH", "DiffAttnError", "SUPPORTED_WIDTHS",
 ]
 
@@ -57,6 +57,8 @@ def load():
     lib.diffattn_decode.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, vp, f32, i32, vp, sz,
                                     vp, vp, vp]
     lib.diffattn_decode.restype = i32
+    lib.diffattn_standard_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
+    lib.diffattn_standard_fwd.restype = i32
     lib.diffattn_status_string.argtypes = [i32]
     lib.diffattn_status_string.restype = ctypes.c_char_p
     lib.diffattn_last_device_error.argtypes = [vp]
@@ -116,6 +118,23 @@ def fwd(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps=1e-5, ou
                                 _ptr(o_prenorm), _stream(stream))
     if rc != OK:
         raise DiffAttnError(rc, "diffattn_fwd")
+    return out
+
+
+def standard_fwd(q, k, v, causal=False, out=None, out_f32=None, stream=None):
+    """Standard softmax attention (the single-map baseline), d = dv = 128.
+    q [B,H,Nq,128], k [B,H,Nk,128], v [B,H,Nk,128] CUDA bf16; returns out."""
+    import torch
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_bf16(n, t)
+    B, H, Nq, d = q.shape
+    Nk, dv = k.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, H, Nq, dv), dtype=torch.bfloat16, device=q.device)
+    rc = load().diffattn_standard_fwd(_ptr(q), _ptr(k), _ptr(v), int(bool(causal)), B, H, Nq, Nk, d, dv,
+                                      _ptr(out), _ptr(out_f32), _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_standard_fwd")
     return out
 
 

@@ -90,6 +90,22 @@ int diffattn_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
                            nullptr, stream);
 }
 
+int diffattn_standard_fwd(const void* q, const void* k, const void* v, int causal, int B, int H, int Nq, int Nk,
+                          int d, int dv, void* out, float* out_f32, void* stream) {
+    if (!q || !k || !v || !out) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
+    if (d != 128 || dv != 128) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(out_f32))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
+    diffattn::StandardArgs a{q, k, v, causal, B, H, Nq, Nk, d, dv, out, out_f32};
+    return from_launch(diffattn::launch_standard(a, static_cast<cudaStream_t>(stream)));
+}
+
 size_t diffattn_decode_workspace_bytes(int B, int H, int Nk, int dv, int num_splits) {
     if (B < 0 || H < 0 || Nk < 1 || dv < 1 || num_splits < 0 || num_splits > kMaxSplits) return 0;
     return workspace_for(B, H, dv, num_splits == 0 ? kMaxAutoSplits : num_splits);

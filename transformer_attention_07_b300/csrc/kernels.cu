@@ -36,6 +36,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int s
 
 #include "decode_sm103a.cuh"
 #include "prefill_sm103a.cuh"
+#include "standard_attn_sm103a.cuh"
 
 namespace diffattn {
 
@@ -121,6 +122,38 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t st) {
     if (a.d == 32 && a.dv == 64)
         return a.causal ? launch_prefill_t<32, 64, true>(a, st) : launch_prefill_t<32, 64, false>(a, st);
     return LAUNCH_ERR_UNSUPPORTED;
+}
+
+// ----------------------------------------------------------------- standard attention
+
+template <bool CAUSAL>
+static int launch_standard_t(const StandardArgs& a, cudaStream_t st) {
+    using L = StandardLayout;
+    CUtensorMap mq, mk, mv;
+    if (!make_map_bhnd(&mq, a.q, a.B, a.H, a.Nq, L::D, 64, L::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bhnd(&mk, a.k, a.B, a.H, a.Nk, L::D, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_bhnd(&mv, a.v, a.B, a.H, a.Nk, L::DV, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        return LAUNCH_ERR_CUDA;
+    StandardParams p;
+    p.B = a.B;
+    p.H = a.H;
+    p.Nq = a.Nq;
+    p.Nk = a.Nk;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)L::D));
+    p.out = static_cast<uint16_t*>(a.out);
+    p.out_f32 = a.out_f32;
+    auto kern = standard_attn_kernel<CAUSAL>;
+    if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
+                 "standard attention: set shared memory"))
+        return LAUNCH_ERR_CUDA;
+    const dim3 grid((a.Nq + 2 * L::BM - 1) / (2 * L::BM), a.H, a.B);
+    kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq, mk, mv, p);
+    return cuda_ok(cudaGetLastError(), "standard attention: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+}
+
+int launch_standard(const StandardArgs& a, cudaStream_t st) {
+    if (a.d != StandardLayout::D || a.dv != StandardLayout::DV) return LAUNCH_ERR_UNSUPPORTED;
+    return a.causal ? launch_standard_t<true>(a, st) : launch_standard_t<false>(a, st);
 }
 
 // ----------------------------------------------------------------- decode

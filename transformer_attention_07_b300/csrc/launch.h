@@ -34,7 +34,15 @@ struct DecodeArgs {
 // reported on stderr (call site and the runtime's error string).
 bool cuda_ok(cudaError_t e, const char* what);
 
+struct StandardArgs {
+    const void *q, *k, *v;
+    int causal, B, H, Nq, Nk, d, dv;
+    void* out;
+    float* out_f32;
+};
+
 int launch_prefill(const PrefillArgs& a, cudaStream_t st);
+int launch_standard(const StandardArgs& a, cudaStream_t st);
 int launch_decode(const DecodeArgs& a, cudaStream_t st);
 int read_and_clear_device_error(cudaStream_t st, int* value);
 

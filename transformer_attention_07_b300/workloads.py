@@ -123,6 +123,20 @@ def make_inputs(w: Workload, device="cuda", seed: int | None = None, Nq: int | N
     return {"q1": q1, "k1": k1, "q2": q2, "k2": k2, "v": v, "gamma": gamma}
 
 
+def standard_inputs(B: int, H: int, N: int, d: int = 128, dv: int = 128, seed: int = 2000, device="cuda"):
+    """q, k, v (bf16, N(0,1)) for the single-map baseline of width d = dv =
+    128: one differential head's [q1; q2] and v at equal parameters."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    return {"q": _randn((B, H, N, d), gen, device), "k": _randn((B, H, N, d), gen, device),
+            "v": _randn((B, H, N, dv), gen, device)}
+
+
+# DiffAttn against the single-map baseline at the sequence lengths the pages
+# quote a throughput overhead for (2K and 4K), with the same token count.
+COMPARE_SHAPES = ((8, 16, 2048), (4, 16, 4096))
+
+
 def plant_needles(q1: torch.Tensor, k1: torch.Tensor, d: int) -> None:
     """In place: the first key of every 256-token block of K1 becomes
     4*sqrt(d) times the unit direction of that block's mean Q1 row, a key

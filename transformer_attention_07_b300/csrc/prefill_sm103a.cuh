@@ -189,10 +189,28 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             constexpr uint32_t idesc_pv = idesc_bf16_f32(L::BM, DV, true);
             bool ok = mbar_wait(bar(L::B_Q), 0, ERR_SITE_PREFILL_MMA);
             tc_fence_after();
-            const uint64_t dq[2] = {smem_desc(sb + L::OFF_Q1, 16, L::QK_SBO, L::QK_SWZ),
-                                    smem_desc(sb + L::OFF_Q2, 16, L::QK_SBO, L::QK_SWZ)};
-            const uint32_t s_col[2] = {L::TM_S1, L::TM_S2};
-            const uint32_t o_col[2] = {L::TM_O1, L::TM_O2};
+            // Operand descriptors are built once; stages and k-steps are
+            // compile-time offsets in the descriptor's address field (units of
+            // 16 bytes), so each MMA costs one add: the issuing thread's own
+            // instruction latency otherwise bounds the tensor pipe.
+            const uint64_t dq1 = smem_desc(sb + L::OFF_Q1, 16, L::QK_SBO, L::QK_SWZ);
+            const uint64_t dq2 = smem_desc(sb + L::OFF_Q2, 16, L::QK_SBO, L::QK_SWZ);
+            const uint64_t dk0 = smem_desc(sb + L::OFF_K, 16, L::QK_SBO, L::QK_SWZ);   // K1 of stage 0
+            const uint64_t dv0 = smem_desc(sb + L::OFF_V, L::V_BOX, 1024, SWZ_128B);   // V of stage 0
+            constexpr uint64_t K2_OFF = L::K_BYTES >> 4, KSTAGE = (2 * L::K_BYTES) >> 4, VSTAGE = L::V_BYTES >> 4;
+            const uint32_t t_s1 = tmem + L::TM_S1, t_s2 = tmem + L::TM_S2;
+            const uint32_t t_o1 = tmem + L::TM_O1, t_o2 = tmem + L::TM_O2;
+            // O += P V over one key tile: 16-key steps, P from TMEM columns 8k.
+            auto pv = [&](uint32_t t_o, uint32_t t_p, uint64_t dvs, uint32_t acc0) {
+#pragma unroll
+                for (int k = 0; k < L::BN / 16; ++k)
+                    mma_ts(t_o, t_p + 8u * k, dvs + (uint64_t)(k * (16 * 128 >> 4)), idesc_pv, k == 0 ? acc0 : 1u);
+            };
+            // S = Q K^T over one key tile: 16-column steps of d (32 bytes).
+            auto qk = [&](uint32_t t_s, uint64_t dq, uint64_t dks) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) mma_ss(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk, k > 0 ? 1u : 0u);
+            };
             for (int j = 0; j <= n_kv && ok; ++j) {
                 const int ks = j % L::KST;
                 if (j < n_kv) {
@@ -206,33 +224,32 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                     ok = mbar_wait(bar(L::B_VFULL + vs), (jv / L::VST) & 1, ERR_SITE_PREFILL_MMA);
                     if (!ok) break;
                 }
-                const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
-                const uint32_t k_base = sb + L::OFF_K + (uint32_t)ks * 2 * L::K_BYTES;
-                for (int r = 0; r < 2; ++r) {
-                    // O_r += P_r V for the previous key tile (P_r sits over S_r).
-                    if (jv >= 0) {
-                        ok = mbar_wait(bar(L::B_PFULL + r), jv & 1, ERR_SITE_PREFILL_MMA);
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int k = 0; k < L::BN / 16; ++k) {
-                            const uint64_t bdesc = smem_desc(vsm + (uint32_t)k * 16 * 128, L::V_BOX, 1024, SWZ_128B);
-                            mma_ts(tmem + o_col[r], tmem + s_col[r] + (uint32_t)k * 8, bdesc, idesc_pv,
-                                   (jv > 0 || k > 0) ? 1u : 0u);
-                        }
-                        if (r == 1) mma_commit(bar(L::B_VEMPTY + vs));
-                    }
-                    // S_r = Q_r K_r^T for this key tile.
-                    if (j < n_kv) {
-                        const uint32_t kr = k_base + (uint32_t)r * L::K_BYTES;
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k) {
-                            const uint64_t bdesc = smem_desc(kr + (uint32_t)k * 32, 16, L::QK_SBO, L::QK_SWZ);
-                            mma_ss(tmem + s_col[r], dq[r] + (uint64_t)(k * 2), bdesc, idesc_qk, k > 0 ? 1u : 0u);
-                        }
-                        mma_commit(bar(L::B_SFULL + r));
-                        if (r == 1) mma_commit(bar(L::B_KEMPTY + ks));
-                    }
+                const uint64_t dvs = dv0 + (uint64_t)vs * VSTAGE;
+                const uint64_t dks = dk0 + (uint64_t)ks * KSTAGE;
+                const uint32_t acc0 = jv > 0 ? 1u : 0u;
+                // map 1: O1 += P1 V (previous tile), then S1 = Q1 K1^T (this tile)
+                if (jv >= 0) {
+                    ok = mbar_wait(bar(L::B_PFULL + 0), jv & 1, ERR_SITE_PREFILL_MMA);
+                    if (!ok) break;
+                    tc_fence_after();
+                    pv(t_o1, t_s1, dvs, acc0);
+                }
+                if (j < n_kv) {
+                    qk(t_s1, dq1, dks);
+                    mma_commit(bar(L::B_SFULL + 0));
+                }
+                // map 2
+                if (jv >= 0) {
+                    ok = mbar_wait(bar(L::B_PFULL + 1), jv & 1, ERR_SITE_PREFILL_MMA);
+                    if (!ok) break;
+                    tc_fence_after();
+                    pv(t_o2, t_s2, dvs, acc0);
+                    mma_commit(bar(L::B_VEMPTY + vs));
+                }
+                if (j < n_kv) {
+                    qk(t_s2, dq2, dks + K2_OFF);
+                    mma_commit(bar(L::B_SFULL + 1));
+                    mma_commit(bar(L::B_KEMPTY + ks));
                 }
             }
             // Always signal the epilogue (also after a failed wait) once every

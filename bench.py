@@ -225,6 +225,56 @@ def compare_single_map(dev, reps=10):
     return res
 
 
+def paged_decode_throughput(dev, reps=10):
+    """Paged split-KV decode on decode_32k-sized caches (B=32, H=32, up to
+    32768 keys, d=64, dv=128) in shuffled pages of 64 keys: all sequences
+    full, then lengths spread over [1024, 32768].  Algorithmic bytes: the
+    K1, K2 and V rows each sequence owns, read once, plus q and out."""
+    import torch
+    import transformer_attention_07_b300 as da
+    B, H, N, P, d, dv = 32, 32, 32768, 64, 64, 128
+    max_pages = N // P
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(3000)
+
+    def pages(width):
+        out = torch.empty((B * max_pages, H, P, width), dtype=torch.bfloat16, device=dev)
+        for i in range(0, B * max_pages, 512):
+            out[i:i + 512].copy_(torch.randn((min(512, B * max_pages - i), H, P, width), generator=gen, device=dev))
+        return out
+
+    k1p, k2p, vp = pages(d), pages(d), pages(dv)
+    q1 = torch.randn((B, H, 1, d), generator=gen, device=dev).to(torch.bfloat16)
+    q2 = torch.randn((B, H, 1, d), generator=gen, device=dev).to(torch.bfloat16)
+    perm = torch.randperm(B * max_pages, generator=torch.Generator().manual_seed(3001))
+    table = perm.view(B, max_pages).to(torch.int32).to(dev)
+    ws = torch.empty(da.decode_workspace_bytes(B, H, N, dv, 0), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, H, 1, dv), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    g = torch.Generator().manual_seed(3002)
+    for name, lens in (("full", [N] * B), ("mixed", torch.randint(1024, N + 1, (B,), generator=g).tolist())):
+        sl = torch.tensor(lens, dtype=torch.int32, device=dev)
+        run = lambda: da.decode_paged(q1, q2, k1p, k2p, vp, table, sl, 0.6, 0.8, workspace=ws, out=out,
+                                      stream=stream)
+        for _ in range(3):
+            run()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        nbytes = H * (sum(lens) * (2 * d + dv) + B * (2 * d + dv)) * 2
+        res[name] = {"ms": ms, "GB/s": nbytes / (ms * 1e-3) / 1e9, "keys": sum(lens)}
+    if da.last_device_error() != 0:
+        raise RuntimeError("device-side error in the paged decode")
+    res["layout"] = f"pages of {P} keys, shuffled block table, B{B} H{H} d{d} dv{dv}"
+    del k1p, k2p, vp
+    return res
+
+
 def run_cuda(args, world, rank, local):
     import torch
     import transformer_attention_07_b300 as da
@@ -366,6 +416,9 @@ def run_cuda(args, world, rank, local):
     line["wall_s_timed"] = wall
     if args.only == "all" and not args.no_compare:
         line["single_map_baseline"] = compare_single_map(dev)
+        del din
+        torch.cuda.empty_cache()
+        line["decode_paged"] = paged_decode_throughput(dev)
     if do_pre and not args.no_cpu_baseline:
         cpu = [pin[k].cpu() for k in names]
         rows = sample_rows_uniform(wp.Nq, args.cpu_rows, 4242)

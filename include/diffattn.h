@@ -127,6 +127,36 @@ int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* 
                     void* out, float* o_prenorm, void* stream);
 
 /*
+ * Paged split-KV decode with per-sequence lengths: the computation of
+ * diffattn_decode (one query per (b, h), no mask) over key/value caches kept
+ * in pages, as a serving system stores them.
+ *   k1_pages, k2_pages [num_pages, H, page_size, d] bf16;
+ *   v_pages            [num_pages, H, page_size, dv] bf16:
+ *                      page p holds page_size consecutive keys of every head.
+ *   block_table        [B, max_pages] int32 (device): the pages of sequence b,
+ *                      in key order; entries past the sequence are ignored.
+ *   seq_lens           [B] int32 (device): keys of sequence b, in
+ *                      [1, max_pages * page_size].
+ *   page_size          a multiple of 32.
+ *   q1, q2 [B,H,1,d]; out [B,H,1,dv] bf16; o_prenorm NULL or fp32 [B,H,1,dv];
+ *   num_splits, workspace, workspace_bytes: as diffattn_decode, sized with
+ *   diffattn_decode_workspace_bytes(B, H, max_pages * page_size, dv, num_splits).
+ * Table entries and lengths live on the device, so the host cannot check
+ * them: a page index outside [0, num_pages) or a length outside the range is
+ * clamped, never dereferenced, and reported by diffattn_last_device_error()
+ * (0x301 page, 0x302 length).  The pages one key range spans are staged in
+ * shared memory: a split count for which one range would span more than 1024
+ * pages is refused (DIFFATTN_ERR_INVALID_ARG; num_splits = 0 avoids it).
+ */
+int diffattn_decode_paged(const void* q1, const void* q2, const void* k1_pages, const void* k2_pages,
+                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens,
+                          int max_pages, int page_size, int num_pages,
+                          float lambda, float lambda_init, int B, int H, int d, int dv,
+                          const float* gn_gamma, float eps, int num_splits,
+                          void* workspace, size_t workspace_bytes,
+                          void* out, float* o_prenorm, void* stream);
+
+/*
  * Split-KV decode that allocates nothing: the same computation and arguments
  * as diffattn_decode, minus the workspace.  (The Differential Transformer
  * pages have no counterpart to this entry point; it exists for callers.)

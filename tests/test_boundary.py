@@ -32,7 +32,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "diffattn_fwd", "diffattn_fwd_ex", "diffattn_decode_workspace_bytes", "diffattn_decode",
-        "diffattn_decode_noalloc", "diffattn_standard_fwd", "diffattn_status_string",
+        "diffattn_decode_noalloc", "diffattn_decode_paged", "diffattn_standard_fwd", "diffattn_status_string",
         "diffattn_last_device_error"])
 
 
@@ -88,6 +88,24 @@ def test_standard_fwd_validation(lib):
     assert std(q=MISALIGNED) == INVALID
     assert std(f32=MISALIGNED) == INVALID
     assert std(Nq=0) == OK
+
+
+def test_decode_paged_validation(lib):
+    def pg(q=FAKE, table=FAKE, lens=FAKE, max_pages=4, page_size=64, num_pages=8, B=1, d=64, dv=128, splits=1,
+           ws=FAKE, ws_bytes=1 << 20):
+        return lib.diffattn_decode_paged(q, q, q, q, q, table, lens, max_pages, page_size, num_pages, 0.5, 0.8, B, 1,
+                                         d, dv, None, 1e-5, splits, ws, ws_bytes, FAKE, None, None)
+    assert pg(table=None) == INVALID
+    assert pg(lens=None) == INVALID
+    assert pg(page_size=48) == INVALID          # not a multiple of 32
+    assert pg(page_size=0) == INVALID
+    assert pg(max_pages=0) == INVALID
+    assert pg(num_pages=0) == INVALID
+    assert pg(d=32, dv=128) == UNSUPPORTED
+    assert pg(table=ctypes.c_void_p(0x10002)) == INVALID
+    assert pg(ws=None) == WORKSPACE
+    assert pg(max_pages=2048, page_size=32, splits=1) == INVALID   # one range would span > 1024 pages
+    assert pg(B=0) == OK
 
 
 def test_decode_workspace_bytes(lib):

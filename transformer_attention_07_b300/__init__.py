@@ -57,6 +57,9 @@ def load():
     lib.diffattn_decode.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, vp, f32, i32, vp, sz,
                                     vp, vp, vp]
     lib.diffattn_decode.restype = i32
+    lib.diffattn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, i32, i32, i32,
+                                          vp, f32, i32, vp, sz, vp, vp, vp]
+    lib.diffattn_decode_paged.restype = i32
     lib.diffattn_standard_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.diffattn_standard_fwd.restype = i32
     lib.diffattn_status_string.argtypes = [i32]
@@ -167,6 +170,37 @@ def decode(q1, k1, q2, k2, v, lam, lam_init, gamma=None, eps=1e-5, num_splits=0,
                                 _stream(stream))
     if rc != OK:
         raise DiffAttnError(rc, "diffattn_decode")
+    return out
+
+
+def decode_paged(q1, q2, k1_pages, k2_pages, v_pages, block_table, seq_lens, lam, lam_init, gamma=None, eps=1e-5,
+                 num_splits=0, workspace=None, out=None, o_prenorm=None, stream=None):
+    """Paged split-KV decode.  q1, q2 [B,H,1,d]; k1_pages, k2_pages
+    [num_pages,H,page_size,d]; v_pages [num_pages,H,page_size,dv] (CUDA bf16);
+    block_table [B,max_pages] and seq_lens [B] CUDA int32.  Returns out."""
+    import torch
+    for n, t in (("q1", q1), ("q2", q2), ("k1_pages", k1_pages), ("k2_pages", k2_pages), ("v_pages", v_pages)):
+        _check_bf16(n, t)
+    for n, t in (("block_table", block_table), ("seq_lens", seq_lens)):
+        if not t.is_cuda or t.dtype != torch.int32 or not t.is_contiguous():
+            raise TypeError(f"{n} must be a contiguous CUDA int32 tensor")
+    B, H, _, d = q1.shape
+    num_pages, _, page_size, _ = k1_pages.shape
+    dv = v_pages.shape[3]
+    max_pages = block_table.shape[1]
+    nbytes = decode_workspace_bytes(B, H, max_pages * page_size, dv, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q1.device)
+    if out is None:
+        out = torch.empty((B, H, 1, dv), dtype=torch.bfloat16, device=q1.device)
+    g = _gamma(gamma, H, dv)
+    rc = load().diffattn_decode_paged(_ptr(q1), _ptr(q2), _ptr(k1_pages), _ptr(k2_pages), _ptr(v_pages),
+                                      _ptr(block_table), _ptr(seq_lens), max_pages, page_size, num_pages,
+                                      float(lam), float(lam_init), B, H, d, dv, _ptr(g), float(eps), int(num_splits),
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+                                      _ptr(o_prenorm), _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_decode_paged")
     return out
 
 

@@ -161,6 +161,56 @@ int diffattn_decode_noalloc(const void* q1, const void* k1, const void* q2, cons
                            scratch, scratch_bytes, out, o_prenorm, stream);
 }
 
+int diffattn_decode_paged(const void* q1, const void* q2, const void* k1_pages, const void* k2_pages,
+                          const void* v_pages, const int32_t* block_table, const int32_t* seq_lens, int max_pages,
+                          int page_size, int num_pages, float lambda, float lambda_init, int B, int H, int d, int dv,
+                          const float* gn_gamma, float eps, int num_splits, void* workspace, size_t workspace_bytes,
+                          void* out, float* o_prenorm, void* stream) {
+    if (!q1 || !q2 || !k1_pages || !k2_pages || !v_pages || !block_table || !seq_lens || !out)
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || d < 1 || dv < 1 || max_pages < 1 || num_pages < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (page_size < 32 || page_size % 32 != 0) return DIFFATTN_ERR_INVALID_ARG;
+    if (num_splits < 0 || num_splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(q2) || !aligned16(k1_pages) || !aligned16(k2_pages) || !aligned16(v_pages) ||
+        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma) || !aligned4(block_table) ||
+        !aligned4(seq_lens))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    // Page caches are addressed as one [num_pages*H*page_size, d] matrix with
+    // 32-bit rows; the longest sequence is max_pages * page_size keys.
+    if ((int64_t)num_pages * H * page_size >= (int64_t(1) << 31) - 64) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)max_pages * page_size >= (int64_t(1) << 31) - 64) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H == 0) return DIFFATTN_OK;
+    const int max_len = max_pages * page_size;
+    // Each key range may span at most kDecodeMaxSplitPages pages.
+    auto pages_ok = [&](int splits) {
+        const int per = ((max_len + splits - 1) / splits + 31) / 32 * 32;
+        return per / page_size + 1 <= diffattn::kDecodeMaxSplitPages;
+    };
+    int splits = num_splits;
+    if (splits == 0) {
+        int dev = 0, sms = 0;
+        if (!diffattn::cuda_ok(cudaGetDevice(&dev), "paged decode: get device") ||
+            !diffattn::cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                               "paged decode: SM count") ||
+            sms < 1)
+            return DIFFATTN_ERR_CUDA;
+        splits = choose_splits((int64_t)B * H, max_len, sms);
+        while (!pages_ok(splits) && splits < kMaxSplits) ++splits;
+    }
+    if (!pages_ok(splits)) return DIFFATTN_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < workspace_for(B, H, dv, splits)) return DIFFATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DIFFATTN_ERR_INVALID_ARG;
+    const int per = (max_len + splits - 1) / splits;
+    const int keys_per_split = (per + 31) / 32 * 32;
+    diffattn::DecodeArgs a{q1, k1_pages, q2, k2_pages, v_pages, lambda, lambda_init, eps, B, H, max_len, d, dv,
+                           splits, keys_per_split, gn_gamma, static_cast<float*>(workspace), out, o_prenorm,
+                           block_table, seq_lens, max_pages, page_size, num_pages};
+    return from_launch(diffattn::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
 const char* diffattn_status_string(int status) {
     switch (status) {
         case DIFFATTN_OK: return "ok";

@@ -24,6 +24,7 @@
 // Noise".)
 #pragma once
 
+#include "launch.h"
 #include "sm103_ptx.cuh"
 
 namespace diffattn {
@@ -36,6 +37,13 @@ struct DecodeParams {
     int keys_per_split;   // multiple of 32
     float scale_log2;     // log2(e) / sqrt(d)
     float* ws;            // [B*H*S][2][DV + 4] partials: m, l, pad, pad, O[DV]
+    // Paged caches only: page p holds page_size consecutive keys of every
+    // head (K rows (p*H + h)*page_size + i of the [num_pages*H*page_size, d]
+    // view; V likewise); sequence b's pages are block_table[b*max_pages + .]
+    // and its length is seq_lens[b].
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int max_pages, page_size, num_pages;
 };
 
 struct MergeParams {
@@ -67,7 +75,9 @@ struct DecodeLayout {
     static constexpr int PART = DV + 4;                 // floats per (map) partial
     static constexpr uint32_t OFF_RED = NST * STAGE;    // NCW x 2 x PART floats
     static constexpr uint32_t OFF_BAR = OFF_RED + NCW * 2 * PART * 4;
-    static constexpr uint32_t USED = OFF_BAR + 2 * NST * 8;
+    static constexpr uint32_t OFF_PAGES = OFF_BAR + 2 * NST * 8;   // paged caches: the split's page indices
+    static constexpr int MAX_SPLIT_PAGES = kDecodeMaxSplitPages;
+    static constexpr uint32_t USED = OFF_PAGES + MAX_SPLIT_PAGES * 4;
     static constexpr uint32_t SMEM_BYTES = USED + 1024;
     static constexpr uint32_t SWZ_BYTES = (D == 64) ? 128 : 64;   // K row = swizzle span
     static_assert(USED + 1024 <= 227u * 1024u, "shared memory");
@@ -111,7 +121,10 @@ __device__ __forceinline__ float dot_row_swizzled(const uint8_t* tile, int r, co
     return acc0 + acc1;
 }
 
-template <int D, int DV>
+// PAGED = false: contiguous caches [B, H, Nk, width].  PAGED = true: paged
+// caches with per-sequence lengths (see DecodeParams); a 32-key chunk never
+// straddles a page because page_size is a multiple of 32.
+template <int D, int DV, bool PAGED>
 __global__ void __launch_bounds__(DecodeLayout<D, DV>::THREADS, 1)
 decode_split_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
                     const DecodeParams p) {
@@ -124,13 +137,38 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_cons
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const size_t bh = (size_t)b * p.H + h;
+    int seq_len = p.Nk;
+    if (PAGED) {
+        // Lengths and pages come from device memory the host cannot check:
+        // out-of-range values are clamped (and reported), never dereferenced.
+        seq_len = p.seq_lens[b];
+        const int cap = p.max_pages * p.page_size;
+        if (seq_len < 1 || seq_len > cap) {
+            if (threadIdx.x == 0) atomicCAS(&g_device_error, 0, ERR_DECODE_BAD_LENGTH);
+            seq_len = min(max(seq_len, 1), cap);
+        }
+    }
     const int key_begin = s * p.keys_per_split;
-    const int key_end = min(p.Nk, key_begin + p.keys_per_split);
+    const int key_end = min(seq_len, key_begin + p.keys_per_split);
     const int nkeys = max(0, key_end - key_begin);
     const int nchunks = (nkeys + L::KC - 1) / L::KC;
+    const int first_page = PAGED ? key_begin / p.page_size : 0;
 
     auto full = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)i; };
     auto empty = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)(L::NST + i); };
+
+    if (PAGED && nkeys > 0) {
+        int* pages = reinterpret_cast<int*>(smem + L::OFF_PAGES);
+        const int npages = (key_end - 1) / p.page_size - first_page + 1;   // <= MAX_SPLIT_PAGES (host check)
+        for (int i = threadIdx.x; i < npages; i += blockDim.x) {
+            int pg = p.block_table[(size_t)b * p.max_pages + first_page + i];
+            if (pg < 0 || pg >= p.num_pages) {
+                atomicCAS(&g_device_error, 0, ERR_DECODE_BAD_PAGE);
+                pg = 0;
+            }
+            pages[i] = pg;
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < L::NST; ++i) {
@@ -148,19 +186,27 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_cons
     if (warp == L::NCW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            const int krow0 = (int)(bh * (size_t)p.Nk) + key_begin;   // row in the [B*H*Nk, D] view
+            const int* pages = reinterpret_cast<const int*>(smem + L::OFF_PAGES);
             int issued = 0;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c % L::NST;
                 if (!mbar_wait(empty(st), ((c / L::NST) & 1) ^ 1, ERR_SITE_DECODE_PRODUCER)) break;
                 const int k0 = key_begin + c * L::KC;
                 const int rows = min(L::KC, key_end - k0);
+                // Row of this chunk's first key in the [rows, D] view of the K
+                // caches (the V cache has the same row order).
+                size_t krow;
+                if (PAGED) {
+                    const int pg = pages[k0 / p.page_size - first_page];
+                    krow = ((size_t)pg * p.H + h) * p.page_size + (k0 % p.page_size);
+                } else {
+                    krow = bh * (size_t)p.Nk + k0;
+                }
                 const uint32_t base = sb + L::OFF_RING + (uint32_t)st * L::STAGE;
                 mbar_arrive_expect_tx(full(st), 2 * L::K_BYTES + (uint32_t)rows * DV * 2);
-                tma_load_4d(base, &tm_k1, full(st), 0, krow0 + c * L::KC, 0, 0);
-                tma_load_4d(base + L::K_BYTES, &tm_k2, full(st), 0, krow0 + c * L::KC, 0, 0);
-                bulk_load(base + 2 * L::K_BYTES, p.v + (bh * (size_t)p.Nk + k0) * DV, (uint32_t)rows * DV * 2,
-                          full(st));
+                tma_load_4d(base, &tm_k1, full(st), 0, (int)krow, 0, 0);
+                tma_load_4d(base + L::K_BYTES, &tm_k2, full(st), 0, (int)krow, 0, 0);
+                bulk_load(base + 2 * L::K_BYTES, p.v + krow * DV, (uint32_t)rows * DV * 2, full(st));
                 ++issued;
             }
             for (int st = 0; st < L::NST && st < issued; ++st) {

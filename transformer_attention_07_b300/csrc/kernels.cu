@@ -158,14 +158,14 @@ int launch_standard(const StandardArgs& a, cudaStream_t st) {
 
 // ----------------------------------------------------------------- decode
 
-template <int D, int DV>
+template <int D, int DV, bool PAGED>
 static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     using L = DecodeLayout<D, DV>;
     // K1/K2 viewed as [B*H*Nk rows, D]: 32-row boxes with the swizzle that
     // matches the row width.
     CUtensorMap mk1, mk2;
     const CUtensorMapSwizzle swz = D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    const int rows = a.B * a.H * a.Nk;
+    const int rows = PAGED ? a.num_pages * a.H * a.page_size : a.B * a.H * a.Nk;
     if (!make_map_bhnd(&mk1, a.k1, 1, 1, rows, D, D, L::KC, swz) ||
         !make_map_bhnd(&mk2, a.k2, 1, 1, rows, D, D, L::KC, swz))
         return LAUNCH_ERR_CUDA;
@@ -180,7 +180,12 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     p.keys_per_split = a.keys_per_split;
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
     p.ws = a.ws;
-    auto kern = decode_split_kernel<D, DV>;
+    p.block_table = a.block_table;
+    p.seq_lens = a.seq_lens;
+    p.max_pages = a.max_pages;
+    p.page_size = a.page_size;
+    p.num_pages = a.num_pages;
+    auto kern = decode_split_kernel<D, DV, PAGED>;
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
                  "decode: set shared memory"))
         return LAUNCH_ERR_CUDA;
@@ -203,8 +208,11 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t st) {
-    if (a.d == 64 && a.dv == 128) return launch_decode_t<64, 128>(a, st);
-    if (a.d == 32 && a.dv == 64) return launch_decode_t<32, 64>(a, st);
+    const bool paged = a.block_table != nullptr;
+    if (a.d == 64 && a.dv == 128)
+        return paged ? launch_decode_t<64, 128, true>(a, st) : launch_decode_t<64, 128, false>(a, st);
+    if (a.d == 32 && a.dv == 64)
+        return paged ? launch_decode_t<32, 64, true>(a, st) : launch_decode_t<32, 64, false>(a, st);
     return LAUNCH_ERR_UNSUPPORTED;
 }
 

@@ -10,6 +10,10 @@ namespace diffattn {
 
 enum LaunchStatus { LAUNCH_OK = 0, LAUNCH_ERR_CUDA = 1, LAUNCH_ERR_UNSUPPORTED = 2 };
 
+// Paged decode: most pages one key range (split) may span; their indices are
+// staged in shared memory.
+constexpr int kDecodeMaxSplitPages = 1024;
+
 struct PrefillArgs {
     const void *q1, *k1, *q2, *k2, *v;
     float lambda, lambda_init, eps;
@@ -28,6 +32,10 @@ struct DecodeArgs {
     float* ws;
     void* out;
     float* o_prenorm;
+    // Paged caches (block_table != nullptr): Nk is then max_pages * page_size.
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int max_pages, page_size, num_pages;
 };
 
 // With DIFFATTN_DEBUG set in the environment, a failing CUDA call is

@@ -25,6 +25,8 @@ enum : int {
     ERR_SITE_DECODE_PRODUCER = 0x201,
     ERR_SITE_DECODE_CONSUMER = 0x202,
     ERR_SITE_DECODE_DRAIN = 0x203,
+    ERR_DECODE_BAD_PAGE = 0x301,      // a block-table entry outside [0, num_pages): clamped, not read
+    ERR_DECODE_BAD_LENGTH = 0x302,    // a sequence length outside [1, max_pages * page_size): clamped
 };
 
 // Upper bound of any single wait.  A legitimate wait lasts microseconds (one

@@ -16,6 +16,10 @@ What it computes (the Differential Transformer pages):
   steps 2-4: the two maps, the lambda-weighted subtraction, GroupNorm of the
   multi-head output and the ``(1 - lambda_init)`` scale.
 
+The backward pass (``diffattn_bwd``) is the chain rule through the same
+steps, one query row at a time; lambda is learnable on the pages, so its
+gradient and that of the GroupNorm gain are returned with the input gradients.
+
 The arithmetic lives in ``oracle.cpp`` (fp64, one row at a time, both
 softmax rows materialised); this module only marshals arrays.
 """
@@ -61,6 +65,10 @@ def _load():
         lib.oracle_diffattn_fwd.restype = i32
         lib.oracle_diffattn_maps.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp]
         lib.oracle_diffattn_maps.restype = i32
+        lib.oracle_diffattn_bwd.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, f64, f64, i32,
+                                            i32, i32, i32, i32, i32, i32, vp, f64,
+                                            vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32]
+        lib.oracle_diffattn_bwd.restype = i32
         _lib = lib
     return _lib
 
@@ -108,12 +116,7 @@ def diffattn_fwd(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps
     (aq1, ak1, aq2, ak2, av), in_type = [a for a, _ in arrs], types.pop()
     B, H, Nq, d = aq1.shape
     Nk, dv = ak1.shape[2], av.shape[3]
-    g = None
-    if gamma is not None:
-        g = np.ascontiguousarray(np.asarray(gamma.cpu() if hasattr(gamma, "cpu") else gamma,
-                                            dtype=np.float64).reshape(-1))
-        if g.size != H * dv:
-            raise ValueError("gamma must have H*dv entries")
+    g = _gamma_array(gamma, H, dv)
     r = None
     R = Nq
     if rows is not None:
@@ -128,6 +131,64 @@ def diffattn_fwd(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps
     if rc != 0:
         raise ValueError("oracle_diffattn_fwd rejected its arguments")
     return o_pre, y
+
+
+def _gamma_array(gamma, H, dv):
+    if gamma is None:
+        return None
+    g = np.ascontiguousarray(np.asarray(gamma.cpu() if hasattr(gamma, "cpu") else gamma,
+                                        dtype=np.float64).reshape(-1))
+    if g.size != H * dv:
+        raise ValueError("gamma must have H*dv entries")
+    return g
+
+
+def diffattn_bwd(q1, k1, q2, k2, v, dy, lam, lam_init, causal=False, gamma=None, eps=1e-5,
+                 rows=None, keys=None, threads=0):
+    """Backward pass in fp64: gradients of ``sum(dy * y)``.
+
+    Inputs as for ``diffattn_fwd``; dy is [B,H,Nq,dv] (any accepted dtype).
+    ``rows`` / ``keys`` optionally restrict the query rows whose dq and the
+    keys whose dk, dv are computed (the same indices for every (b,h)).
+    Returns a dict of float64 arrays: dq1, dq2 [B,H,R,d]; dk1, dk2 [B,H,K,d];
+    dv [B,H,K,dv]; and, only when neither rows nor keys is given, dlambda
+    (a float) and dgamma [H*dv].
+    """
+    arrs = [_as_input(t) for t in (q1, k1, q2, k2, v)]
+    types = {t for _, t in arrs}
+    if len(types) != 1:
+        raise TypeError("q1,k1,q2,k2,v must share one dtype")
+    (aq1, ak1, aq2, ak2, av), in_type = [a for a, _ in arrs], types.pop()
+    ady, dy_type = _as_input(dy)
+    B, H, Nq, d = aq1.shape
+    Nk, dv = ak1.shape[2], av.shape[3]
+    if ady.shape != (B, H, Nq, dv):
+        raise ValueError("dy must be [B,H,Nq,dv]")
+    g = _gamma_array(gamma, H, dv)
+    r = k = None
+    R, K = Nq, Nk
+    if rows is not None:
+        r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        R = r.size
+    if keys is not None:
+        k = np.ascontiguousarray(np.asarray(keys, dtype=np.int64).reshape(-1))
+        K = k.size
+    full = rows is None and keys is None
+    out = {"dq1": np.empty((B, H, R, d)), "dq2": np.empty((B, H, R, d)), "dk1": np.empty((B, H, K, d)),
+           "dk2": np.empty((B, H, K, d)), "dv": np.empty((B, H, K, dv))}
+    dlam = np.zeros(1) if full else None
+    dgam = np.empty(H * dv) if full else None
+    rc = _load().oracle_diffattn_bwd(
+        _ptr(aq1), _ptr(ak1), _ptr(aq2), _ptr(ak2), _ptr(av), in_type, _ptr(ady), dy_type,
+        float(lam), float(lam_init), int(bool(causal)), B, H, Nq, Nk, d, dv, _ptr(g), float(eps),
+        _ptr(r), R, _ptr(k), K, _ptr(out["dq1"]), _ptr(out["dq2"]), _ptr(out["dk1"]), _ptr(out["dk2"]),
+        _ptr(out["dv"]), _ptr(dlam), _ptr(dgam), int(threads))
+    if rc != 0:
+        raise ValueError("oracle_diffattn_bwd rejected its arguments")
+    if full:
+        out["dlambda"] = float(dlam[0])
+        out["dgamma"] = dgam
+    return out
 
 
 def diffattn_maps(q1, k1, q2, k2, causal=False):

@@ -1,0 +1,134 @@
+"""Pins for the oracle's backward pass (CPU only).
+
+The oracle's gradients are checked against two things outside it:
+
+* central finite differences of the oracle's own forward pass (a check of
+  the derivative, not of a retyped formula: a dropped term, a wrong sign, a
+  swapped operand or a wrong index in the chain rule changes the result), for
+  every element of every input, and for lambda and the GroupNorm gain;
+* torch autograd through library routines (``scaled_dot_product_attention``
+  for each map and ``group_norm``), in float64.
+
+Plus the row/key subsetting of the oracle against its own full result.
+"""
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def problem(B, H, Nq, Nk, d, dv, seed):
+    rng = np.random.default_rng(seed)
+    q1, q2 = rng.standard_normal((B, H, Nq, d)), rng.standard_normal((B, H, Nq, d))
+    k1, k2 = rng.standard_normal((B, H, Nk, d)), rng.standard_normal((B, H, Nk, d))
+    v = rng.standard_normal((B, H, Nk, dv))
+    dy = rng.standard_normal((B, H, Nq, dv))
+    gamma = rng.random(H * dv) + 0.5
+    return {"q1": q1, "k1": k1, "q2": q2, "k2": k2, "v": v}, dy, gamma
+
+
+def loss(t, dy, lam, lam_init, causal, gamma):
+    _, y = oracle.diffattn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], lam, lam_init, causal=causal,
+                               gamma=gamma, threads=1)
+    return float((y * dy).sum())
+
+
+@pytest.mark.parametrize("causal,Nq,Nk", [(False, 5, 6), (True, 6, 6), (True, 4, 7)])
+def test_gradients_match_finite_differences(causal, Nq, Nk):
+    B, H, d, dv = 1, 2, 4, 6
+    t, dy, gamma = problem(B, H, Nq, Nk, d, dv, seed=Nq * 10 + Nk + causal)
+    lam, lam_init, h = 0.6, 0.8, 1e-5
+    g = oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, lam, lam_init, causal=causal,
+                            gamma=gamma, threads=1)
+    for name in ("q1", "k1", "q2", "k2", "v"):
+        num = np.zeros_like(t[name])
+        for idx in np.ndindex(t[name].shape):
+            orig = t[name][idx]
+            t[name][idx] = orig + h
+            lp = loss(t, dy, lam, lam_init, causal, gamma)
+            t[name][idx] = orig - h
+            lm = loss(t, dy, lam, lam_init, causal, gamma)
+            t[name][idx] = orig
+            num[idx] = (lp - lm) / (2 * h)
+        assert np.abs(g["d" + name] - num).max() < 1e-7 * max(1.0, np.abs(num).max()), name
+    num_lam = (loss(t, dy, lam + h, lam_init, causal, gamma) - loss(t, dy, lam - h, lam_init, causal, gamma)) / (2 * h)
+    assert abs(g["dlambda"] - num_lam) < 1e-7 * max(1.0, abs(num_lam))
+    num_g = np.zeros_like(gamma)
+    for c in range(gamma.size):
+        gp, gm = gamma.copy(), gamma.copy()
+        gp[c] += h
+        gm[c] -= h
+        num_g[c] = (loss(t, dy, lam, lam_init, causal, gp) - loss(t, dy, lam, lam_init, causal, gm)) / (2 * h)
+    assert np.abs(g["dgamma"] - num_g).max() < 1e-7 * max(1.0, np.abs(num_g).max())
+
+
+def torch_forward(q1, k1, q2, k2, v, lam, lam_init, causal, gamma, eps):
+    """The forward pass assembled from library routines (float64)."""
+    B, H, Nq, _ = q1.shape
+    Nk, dv = k1.shape[2], v.shape[3]
+    mask = None
+    if causal:   # key j visible to query i iff j <= i + Nk - Nq
+        i = torch.arange(Nq)[:, None]
+        j = torch.arange(Nk)[None, :]
+        mask = j <= i + (Nk - Nq)
+    a1v = F.scaled_dot_product_attention(q1, k1, v, attn_mask=mask)
+    a2v = F.scaled_dot_product_attention(q2, k2, v, attn_mask=mask)
+    o = a1v - lam * a2v
+    x = o.permute(0, 2, 1, 3).reshape(B * Nq, H * dv)
+    y = F.group_norm(x, H, weight=gamma, bias=None, eps=eps) * (1 - lam_init)
+    return y.reshape(B, Nq, H, dv).permute(0, 2, 1, 3)
+
+
+@pytest.mark.parametrize("causal,Nq,Nk", [(False, 37, 41), (True, 37, 41), (True, 33, 33)])
+def test_gradients_match_torch_autograd(causal, Nq, Nk):
+    B, H, d, dv = 2, 3, 8, 16
+    t, dy, gamma = problem(B, H, Nq, Nk, d, dv, seed=7 + Nq + causal)
+    lam, lam_init, eps = -0.3 if causal else 0.9, 0.7, 1e-5
+    tt = {k: torch.tensor(x, requires_grad=True) for k, x in t.items()}
+    tlam = torch.tensor(lam, dtype=torch.float64, requires_grad=True)
+    tg = torch.tensor(gamma, requires_grad=True)
+    y = torch_forward(tt["q1"], tt["k1"], tt["q2"], tt["k2"], tt["v"], tlam, lam_init, causal, tg, eps)
+    (y * torch.tensor(dy)).sum().backward()
+    g = oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, lam, lam_init, causal=causal,
+                            gamma=gamma, eps=eps)
+    for name in ("q1", "k1", "q2", "k2", "v"):
+        ref = tt[name].grad.numpy()
+        assert np.abs(g["d" + name] - ref).max() < 1e-10 * max(1.0, np.abs(ref).max()), name
+    assert abs(g["dlambda"] - tlam.grad.item()) < 1e-10 * max(1.0, abs(tlam.grad.item()))
+    assert np.abs(g["dgamma"] - tg.grad.numpy()).max() < 1e-10 * max(1.0, np.abs(tg.grad.numpy()).max())
+
+
+def test_row_and_key_subsets_equal_the_full_result():
+    B, H, Nq, Nk, d, dv = 2, 2, 29, 35, 8, 16
+    t, dy, gamma = problem(B, H, Nq, Nk, d, dv, seed=3)
+    args = (t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, 0.5, 0.8)
+    full = oracle.diffattn_bwd(*args, causal=True, gamma=gamma)
+    rows, keys = [0, 7, 28], [1, 30, 34]
+    sub = oracle.diffattn_bwd(*args, causal=True, gamma=gamma, rows=rows, keys=keys)
+    for n in ("dq1", "dq2"):
+        np.testing.assert_allclose(sub[n], full[n][:, :, rows], rtol=0, atol=1e-13)
+    for n in ("dk1", "dk2", "dv"):
+        np.testing.assert_allclose(sub[n], full[n][:, :, keys], rtol=0, atol=1e-13)
+    assert "dlambda" not in sub and "dgamma" not in sub
+
+
+def test_gradients_vanish_when_lambda_init_is_one():
+    """With lambda_init = 1 the output scale (1 - lambda_init) is 0, so y = 0 for
+    every input and every gradient is exactly 0."""
+    t, dy, gamma = problem(1, 2, 9, 9, 4, 8, seed=5)
+    g = oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, 0.4, 1.0, causal=True, gamma=gamma)
+    for n in ("dq1", "dq2", "dk1", "dk2", "dv", "dgamma"):
+        assert np.abs(g[n]).max() == 0.0, n
+    assert g["dlambda"] == 0.0
+
+
+def test_bwd_rejects_bad_arguments():
+    t, dy, _ = problem(1, 1, 4, 4, 4, 8, seed=1)
+    with pytest.raises(ValueError):
+        oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy[:, :, :3], 0.5, 0.8)
+    with pytest.raises(ValueError):
+        oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, 0.5, 0.8, rows=[4])

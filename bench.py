@@ -275,6 +275,44 @@ def paged_decode_throughput(dev, reps=10):
     return res
 
 
+def backward_throughput(dev, w, inp, reps=3):
+    """Backward pass (prep, dQ sweep, dK/dV sweep, finalize) on workload w,
+    after one training forward.  Algorithmic flops per pair 12d + 4dv (S1,
+    S2 recomputed; dP; dV; dK1, dK2; dQ1, dQ2)."""
+    import torch
+    import transformer_attention_07_b300 as da
+    from transformer_attention_07_b300.workloads import make_dy
+    stream = torch.cuda.current_stream(dev)
+    names = ("q1", "k1", "q2", "k2", "v")
+    q1, k1, q2, k2, v = (inp[k] for k in names)
+    _, saved = da.fwd_train(q1, k1, q2, k2, v, w.lam, w.lam_init, causal=w.causal, gamma=inp["gamma"], eps=w.eps,
+                            stream=stream)
+    dy = make_dy(w, device=dev)
+    ws = torch.empty(da.bwd_workspace_bytes(w.B, w.H, w.Nq, w.dv), dtype=torch.uint8, device=dev)
+    grads = {"dq1": torch.empty_like(q1), "dk1": torch.empty_like(k1), "dq2": torch.empty_like(q2),
+             "dk2": torch.empty_like(k2), "dv": torch.empty_like(v),
+             "dlambda": torch.empty(1, dtype=torch.float32, device=dev),
+             "dgamma": torch.empty(w.H * w.dv, dtype=torch.float32, device=dev)}
+    run = lambda: da.bwd(q1, k1, q2, k2, v, dy, saved, w.lam, w.lam_init, causal=w.causal, gamma=inp["gamma"],
+                         eps=w.eps, workspace=ws, grads=grads, stream=stream)
+    for _ in range(2):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if da.last_device_error() != 0:
+        raise RuntimeError("device-side error in the backward pass")
+    ms = e0.elapsed_time(e1) / reps
+    tflops = w.bwd_flops / (ms * 1e-3) / 1e12
+    peak, _, _, src = load_peaks()
+    del saved, dy, ws, grads
+    return {"workload": w.name, "ms": ms, "TFLOP/s": tflops, "flops_per_pair": 12 * w.d + 4 * w.dv,
+            "frac": tflops / peak, "peak": peak, "peak_source": f"{src} burst", "launches_per_call": 4}
+
+
 def run_cuda(args, world, rank, local):
     import torch
     import transformer_attention_07_b300 as da
@@ -287,7 +325,7 @@ def run_cuda(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     wp, wd = WORKLOADS[args.prefill_workload], WORKLOADS[args.decode_workload]
-    do_pre, do_dec = args.only in ("all", "prefill"), args.only in ("all", "decode")
+    do_pre, do_dec = args.only in ("all", "prefill", "backward"), args.only in ("all", "decode")
     # Each rank its own independent problem (seed offset by rank).
     pin = make_inputs(wp, device=dev, seed=rank_seed(wp.seed, rank)) if do_pre else None
     din = make_inputs(wd, device=dev, seed=rank_seed(wd.seed, rank)) if do_dec else None
@@ -296,6 +334,10 @@ def run_cuda(args, world, rank, local):
     ws = torch.empty(da.decode_workspace_bytes(wd.B, wd.H, wd.Nk, wd.dv, 0), dtype=torch.uint8,
                      device=dev) if do_dec else None
     stream = torch.cuda.current_stream(dev)
+    if args.only == "backward":
+        # Profiling mode: the backward pass alone (warm-up 2, then --steps calls).
+        print(json.dumps({"backward": backward_throughput(dev, wp, pin, reps=args.steps)}), flush=True)
+        return 0
 
     def prefill():
         if do_pre:
@@ -419,6 +461,7 @@ def run_cuda(args, world, rank, local):
         del din
         torch.cuda.empty_cache()
         line["decode_paged"] = paged_decode_throughput(dev)
+        line["backward"] = backward_throughput(dev, wp, pin)
     if do_pre and not args.no_cpu_baseline:
         cpu = [pin[k].cpu() for k in names]
         rows = sample_rows_uniform(wp.Nq, args.cpu_rows, 4242)
@@ -446,7 +489,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the DiffAttn vs single-map (standard attention) comparison")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward"], default="all",
                     help="run one stage per step (profiling of a single kernel)")
     ap.add_argument("--prefill-workload", default=PREFILL)
     ap.add_argument("--decode-workload", default=DECODE)

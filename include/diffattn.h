@@ -1,5 +1,5 @@
 /*
- * diffattn.h — C ABI of the B300 (sm_103a) differential-attention forward.
+ * diffattn.h — C ABI of the B300 (sm_103a) differential-attention forward and backward.
  *
  * The operation (Differential Transformer pages):
  *   "How does Differential Attention work to suppress noise and improve
@@ -80,6 +80,57 @@ int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* 
                     float lambda, float lambda_init, int causal,
                     int B, int H, int Nq, int Nk, int d, int dv,
                     const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream);
+
+/*
+ * Training forward: diffattn_fwd_ex plus what the backward pass reads.
+ *   o_prenorm   [B,H,Nq,dv] fp32, required: (A1 - lambda A2) V
+ *   o2          [B,H,Nq,dv] fp32, required, 16-byte aligned: A2 V
+ *   lse         [2,B,H,Nq] fp32, required, 4-byte aligned: for map r and row
+ *               i, log sum_j exp(q_r,i . k_r,j / sqrt d) over the visible keys
+ *               (natural log); map 1 first
+ * Other arguments, checks and statuses as diffattn_fwd.
+ */
+int diffattn_fwd_train(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                       float lambda, float lambda_init, int causal,
+                       int B, int H, int Nq, int Nk, int d, int dv,
+                       const float* gn_gamma, float eps, void* out,
+                       float* o_prenorm, float* o2, float* lse, void* stream);
+
+/*
+ * Bytes of device workspace diffattn_bwd needs (0 for invalid sizes).
+ */
+size_t diffattn_bwd_workspace_bytes(int B, int H, int Nq, int dv);
+
+/*
+ * Backward pass: the gradients of a loss L with respect to every input of
+ * the forward pass, given dy = dL/dy.  lambda is learnable on the pages (the
+ * iloveeagents.com Q&A, "Mathematical Formula"), so dL/dlambda is returned
+ * with the GroupNorm gain's gradient and the five input gradients:
+ *   do      = GroupNorm backward of dy (per row, through gamma and (1 - lambda_init))
+ *   dS1     = A1 o (do V^T - rowsum(A1 o do V^T)),  dS2 = -lambda A2 o (do V^T - rowsum(...))
+ *   dq_r    = dS_r k_r / sqrt d,   dk_r = dS_r^T q_r / sqrt d,   dv = (A1 - lambda A2)^T do
+ *   dlambda = -sum do . (A2 V),    dgamma = (1 - lambda_init) sum_rows dy o xhat
+ * Inputs: q1, k1, q2, k2, v, lambda, lambda_init, causal, gn_gamma, eps as in
+ *   the forward call; dy [B,H,Nq,dv] bf16; o_prenorm, o2, lse as written by
+ *   diffattn_fwd_train for those inputs.
+ * Outputs (bf16, the inputs' shapes): dq1, dq2 [B,H,Nq,d]; dk1, dk2 [B,H,Nk,d];
+ *   dv_grad [B,H,Nk,dv].  dlambda (one float) and dgamma ([H*dv] fp32) may be
+ *   NULL when not wanted; dlambda sums over every (b, h, i).
+ * workspace: >= diffattn_bwd_workspace_bytes(B, H, Nq, dv) bytes, 256-byte
+ *   aligned, no initialisation needed; concurrent calls need separate ones.
+ * Supported widths: (d, dv) = (64, 128).  Other widths return
+ * DIFFATTN_ERR_UNSUPPORTED.  Nq = 0 writes zero key gradients (the
+ * query-side pointers may then be NULL).  Results are
+ * deterministic: no atomics, fixed summation orders.
+ */
+int diffattn_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                 const void* dy, const float* o_prenorm, const float* o2, const float* lse,
+                 float lambda, float lambda_init, int causal,
+                 int B, int H, int Nq, int Nk, int d, int dv,
+                 const float* gn_gamma, float eps,
+                 void* dq1, void* dk1, void* dq2, void* dk2, void* dv_grad,
+                 float* dlambda, float* dgamma,
+                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Standard softmax attention, the single-map baseline the pages compare

@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "diffattn_fwd", "diffattn_fwd_ex", "diffattn_decode_workspace_bytes", "diffattn_decode",
+        "diffattn_fwd", "diffattn_fwd_ex", "diffattn_fwd_train", "diffattn_bwd_workspace_bytes", "diffattn_bwd",
+        "diffattn_decode_workspace_bytes", "diffattn_decode",
         "diffattn_decode_noalloc", "diffattn_decode_paged", "diffattn_standard_fwd", "diffattn_status_string",
         "diffattn_last_device_error"])
 
@@ -75,6 +76,47 @@ def test_fwd_empty_problems_return_ok_without_launch(lib):
     assert fwd(lib, H=0) == OK
     assert fwd(lib, Nq=0) == OK
     assert fwd(lib, Nq=0, causal=1) == OK
+
+
+def test_fwd_train_validation(lib):
+    tr = lambda o2=FAKE, lse=FAKE, pre=FAKE, d=64, dv=128, B=1: lib.diffattn_fwd_train(
+        FAKE, FAKE, FAKE, FAKE, FAKE, 0.5, 0.8, 0, B, 1, 4, 4, d, dv, None, 1e-5, FAKE, pre, o2, lse, None)
+    assert tr(o2=None) == INVALID
+    assert tr(lse=None) == INVALID
+    assert tr(pre=None) == INVALID
+    assert tr(o2=MISALIGNED) == INVALID
+    assert tr(lse=ctypes.c_void_p(0x10002)) == INVALID
+    assert tr(d=64, dv=64) == UNSUPPORTED
+    assert tr(B=0) == OK
+
+
+def test_bwd_workspace_bytes(lib):
+    ws = lib.diffattn_bwd_workspace_bytes
+    align = lambda x: (x + 255) // 256 * 256
+    # do (bf16) + per-row constants (Nq rounded up to 128) + partial sums per 64 rows
+    B, H, Nq, dv = 2, 3, 200, 128
+    pad = 256
+    assert ws(B, H, Nq, dv) == (align(B * H * Nq * dv * 2) + align(B * H * pad * 16) +
+                                align(B * H * (pad // 64) * dv * 4) + align(B * H * (pad // 64) * 4))
+    assert ws(-1, 1, 1, 128) == 0
+
+
+def test_bwd_validation(lib):
+    def bwd(q=FAKE, d=64, dv=128, causal=0, Nq=4, Nk=4, ws=ctypes.c_void_p(0x10000), ws_bytes=1 << 20, dl=None,
+            grad=FAKE, B=1):
+        return lib.diffattn_bwd(q, q, q, q, q, q, q, q, q, 0.5, 0.8, causal, B, 1, Nq, Nk, d, dv, None, 1e-5,
+                                grad, grad, grad, grad, grad, dl, None, ws, ws_bytes, None)
+    assert bwd(q=None) == INVALID
+    assert bwd(grad=None) == INVALID
+    assert bwd(Nk=0) == INVALID
+    assert bwd(causal=1, Nq=5, Nk=4) == INVALID
+    assert bwd(d=32, dv=64) == UNSUPPORTED
+    assert bwd(q=MISALIGNED) == INVALID
+    assert bwd(dl=ctypes.c_void_p(0x10002)) == INVALID
+    assert bwd(ws=None) == WORKSPACE
+    assert bwd(ws_bytes=16) == WORKSPACE
+    assert bwd(ws=ctypes.c_void_p(0x10010)) == INVALID     # not 256-byte aligned
+    assert bwd(B=0) == OK
 
 
 def test_standard_fwd_validation(lib):

@@ -18,8 +18,9 @@ import ctypes
 import os
 
 __all__ = [
-    "fwd", "standard_fwd", "decode", "decode_workspace_bytes", "status_string", "last_device_error",
-    "load", "LIB_PATH", "DiffAttnError", "SUPPORTED_WIDTHS",
+    "fwd", "fwd_train", "bwd", "bwd_workspace_bytes", "standard_fwd", "decode", "decode_paged",
+    "decode_workspace_bytes", "status_string", "last_device_error", "load", "LIB_PATH", "DiffAttnError",
+    "SUPPORTED_WIDTHS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdiffattn.so")
@@ -60,6 +61,14 @@ def load():
     lib.diffattn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, i32, i32, i32,
                                           vp, f32, i32, vp, sz, vp, vp, vp]
     lib.diffattn_decode_paged.restype = i32
+    lib.diffattn_fwd_train.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32, vp, f32,
+                                       vp, vp, vp, vp, vp]
+    lib.diffattn_fwd_train.restype = i32
+    lib.diffattn_bwd_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    lib.diffattn_bwd_workspace_bytes.restype = sz
+    lib.diffattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32,
+                                 vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    lib.diffattn_bwd.restype = i32
     lib.diffattn_standard_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.diffattn_standard_fwd.restype = i32
     lib.diffattn_status_string.argtypes = [i32]
@@ -122,6 +131,66 @@ def fwd(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps=1e-5, ou
     if rc != OK:
         raise DiffAttnError(rc, "diffattn_fwd")
     return out
+
+
+def fwd_train(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps=1e-5, out=None, stream=None):
+    """Training forward: returns ``(out, saved)`` where ``saved`` holds what
+    ``bwd`` reads: ``o_prenorm`` and ``o2`` (fp32 [B,H,Nq,dv]: (A1 - lambda A2) V
+    and A2 V) and ``lse`` (fp32 [2,B,H,Nq]: each map's log-sum-exp)."""
+    import torch
+    for n, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2), ("v", v)):
+        _check_bf16(n, t)
+    B, H, Nq, d = q1.shape
+    Nk, dv = k1.shape[2], v.shape[3]
+    dev = q1.device
+    if out is None:
+        out = torch.empty((B, H, Nq, dv), dtype=torch.bfloat16, device=dev)
+    saved = {"o_prenorm": torch.empty((B, H, Nq, dv), dtype=torch.float32, device=dev),
+             "o2": torch.empty((B, H, Nq, dv), dtype=torch.float32, device=dev),
+             "lse": torch.empty((2, B, H, Nq), dtype=torch.float32, device=dev)}
+    g = _gamma(gamma, H, dv)
+    rc = load().diffattn_fwd_train(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), float(lam), float(lam_init),
+                                   int(bool(causal)), B, H, Nq, Nk, d, dv, _ptr(g), float(eps), _ptr(out),
+                                   _ptr(saved["o_prenorm"]), _ptr(saved["o2"]), _ptr(saved["lse"]), _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_fwd_train")
+    return out, saved
+
+
+def bwd_workspace_bytes(B, H, Nq, dv) -> int:
+    return int(load().diffattn_bwd_workspace_bytes(B, H, Nq, dv))
+
+
+def bwd(q1, k1, q2, k2, v, dy, saved, lam, lam_init, causal=False, gamma=None, eps=1e-5, workspace=None,
+        grads=None, stream=None):
+    """Backward pass.  ``saved`` is the dict ``fwd_train`` returned for these
+    inputs; dy is the bf16 gradient of the output.  Returns a dict with dq1,
+    dk1, dq2, dk2, dv (bf16, the inputs' shapes), dlambda (fp32 [1]) and
+    dgamma (fp32 [H*dv]); ``grads`` may supply those tensors."""
+    import torch
+    for n, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2), ("v", v), ("dy", dy)):
+        _check_bf16(n, t)
+    B, H, Nq, d = q1.shape
+    Nk, dv = k1.shape[2], v.shape[3]
+    dev = q1.device
+    if grads is None:
+        grads = {"dq1": torch.empty_like(q1), "dk1": torch.empty_like(k1), "dq2": torch.empty_like(q2),
+                 "dk2": torch.empty_like(k2), "dv": torch.empty_like(v),
+                 "dlambda": torch.empty(1, dtype=torch.float32, device=dev),
+                 "dgamma": torch.empty(H * dv, dtype=torch.float32, device=dev)}
+    nbytes = bwd_workspace_bytes(B, H, Nq, dv)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    g = _gamma(gamma, H, dv)
+    rc = load().diffattn_bwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), _ptr(dy), _ptr(saved["o_prenorm"]),
+                             _ptr(saved["o2"]), _ptr(saved["lse"]), float(lam), float(lam_init), int(bool(causal)),
+                             B, H, Nq, Nk, d, dv, _ptr(g), float(eps), _ptr(grads["dq1"]), _ptr(grads["dk1"]),
+                             _ptr(grads["dq2"]), _ptr(grads["dk2"]), _ptr(grads["dv"]), _ptr(grads.get("dlambda")),
+                             _ptr(grads.get("dgamma")), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_bwd")
+    return grads
 
 
 def standard_fwd(q, k, v, causal=False, out=None, out_f32=None, stream=None):

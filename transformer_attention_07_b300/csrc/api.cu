@@ -79,8 +79,78 @@ int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* 
     if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
     if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
     diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
-                            gn_gamma, out, o_prenorm};
+                            gn_gamma, out, o_prenorm, nullptr, nullptr};
     return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+int diffattn_fwd_train(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                       float lambda, float lambda_init, int causal, int B, int H, int Nq, int Nk, int d, int dv,
+                       const float* gn_gamma, float eps, void* out, float* o_prenorm, float* o2, float* lse,
+                       void* stream) {
+    if (!o_prenorm || !o2 || !lse) return DIFFATTN_ERR_INVALID_ARG;
+    if (!aligned16(o2) || !aligned4(lse)) return DIFFATTN_ERR_INVALID_ARG;
+    // Every other check is that of the inference entry point.
+    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
+    diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
+                            gn_gamma, out, o_prenorm, o2, lse};
+    return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t diffattn_bwd_workspace_bytes(int B, int H, int Nq, int dv) {
+    if (B < 0 || H < 0 || Nq < 0 || dv < 1) return 0;
+    return diffattn::bwd_workspace_layout(B, H, Nq, dv).total;
+}
+
+int diffattn_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, const void* dy,
+                 const float* o_prenorm, const float* o2, const float* lse, float lambda, float lambda_init,
+                 int causal, int B, int H, int Nq, int Nk, int d, int dv, const float* gn_gamma, float eps,
+                 void* dq1, void* dk1, void* dq2, void* dk2, void* dv_grad, float* dlambda, float* dgamma,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    // With no query rows the query-side tensors are empty and may be NULL.
+    const bool rows = Nq != 0;
+    if (!k1 || !k2 || !v || !dk1 || !dk2 || !dv_grad) return DIFFATTN_ERR_INVALID_ARG;
+    if (rows && (!q1 || !q2 || !dy || !o_prenorm || !o2 || !lse || !dq1 || !dq2)) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
+    if (!(d == 64 && dv == 128)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(dy) || !aligned16(o_prenorm) || !aligned16(o2) || !aligned4(lse) || !aligned4(gn_gamma) ||
+        !aligned16(dq1) || !aligned16(dk1) || !aligned16(dq2) || !aligned16(dk2) || !aligned16(dv_grad) ||
+        !aligned4(dlambda) || !aligned4(dgamma))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    if (!fits_tensor_map(H, Nq, dv) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
+    const diffattn::BwdWorkspace w = diffattn::bwd_workspace_layout(B, H, Nq, dv);
+    if ((int64_t)B * H == 0) return DIFFATTN_OK;
+    if (!workspace || workspace_bytes < w.total) return DIFFATTN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DIFFATTN_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (Nq == 0) {
+        // No query rows: every key gradient is zero and so are dlambda and dgamma.
+        const size_t kd = (size_t)B * H * Nk * d * 2, kv = (size_t)B * H * Nk * dv * 2;
+        if (cudaMemsetAsync(dk1, 0, kd, st) != cudaSuccess || cudaMemsetAsync(dk2, 0, kd, st) != cudaSuccess ||
+            cudaMemsetAsync(dv_grad, 0, kv, st) != cudaSuccess ||
+            (dlambda && cudaMemsetAsync(dlambda, 0, sizeof(float), st) != cudaSuccess) ||
+            (dgamma && cudaMemsetAsync(dgamma, 0, (size_t)H * dv * sizeof(float), st) != cudaSuccess))
+            return DIFFATTN_ERR_CUDA;
+        return DIFFATTN_OK;
+    }
+    diffattn::BwdArgs a{q1, k1, q2, k2, v, dy, o_prenorm, o2, lse, lambda, lambda_init, eps, causal, B, H, Nq, Nk,
+                        d, dv, gn_gamma, dq1, dk1, dq2, dk2, dv_grad, dlambda, dgamma, workspace};
+    return from_launch(diffattn::launch_backward(a, st));
 }
 
 int diffattn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, float lambda,

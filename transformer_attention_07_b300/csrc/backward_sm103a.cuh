@@ -1,0 +1,768 @@
+// Differential-attention backward pass for sm_103a.
+//
+// The forward pass (Differential Transformer pages: the DiffAttn formula of
+// the iloveeagents.com Q&A, "Mathematical Formula", where lambda is a
+// learnable scalar; steps 2-4 of llmbytes.dev "How Differential Attention
+// Cancels Common-Mode Noise") is, per head and query row i,
+//     o_i = sum_j (A1_ij - lambda A2_ij) v_j,   A_r = softmax(s Q_r K_r^T), s = 1/sqrt(d)
+//     y_i = (1 - lambda_init) gamma * (o_i - mu_i) * rstd_i.
+// Given dy = dL/dy, the chain rule in reverse order gives
+//     do_i    = rstd (g - mean(g) - xhat mean(g xhat)),  g = (1 - lambda_init) gamma dy
+//     dgamma  = (1 - lambda_init) sum_i dy_i xhat_i
+//     dP_ij   = do_i . v_j                     (shared by both maps)
+//     D1_i    = do_i . (A1 V)_i,  D2_i = do_i . (A2 V)_i
+//     dS1_ij  = A1_ij (dP_ij - D1_i),   dS2_ij = -lambda A2_ij (dP_ij - D2_i)
+//     dV_j    = sum_i (A1_ij - lambda A2_ij) do_i
+//     dQ_r,i  = s sum_j dS_r,ij k_r,j,    dK_r,j = s sum_i dS_r,ij q_r,i
+//     dlambda = -sum_i D2_i.
+// The forward stores each map's log-sum-exp and A2 V, so both maps' rows
+// A_r,ij = exp(s q_r,i . k_r,j - lse_r,i) are recomputed tile by tile and no
+// N x N matrix is ever formed.
+//
+// Four kernels:
+//   bwd_prep_kernel     one warp per row: GroupNorm backward, do (bf16),
+//                       D1, D2, per-row constants for the tile kernels, and
+//                       fixed-order partial sums of dgamma and dlambda.
+//   bwd_dq_kernel       one CTA per 128 query rows; walks the key tiles:
+//                       S_r = Q_r K_r^T, dP = dO V^T on the tensor core,
+//                       dS_r in registers, dQ_r += dS_r K_r (dS_r from TMEM).
+//   bwd_dkv_kernel      one CTA per 128 keys; walks the query tiles:
+//                       S_r^T = K_r Q_r^T, dP^T = V dO^T, then
+//                       dV += (A1 - lambda A2)^T dO, dK_r += dS_r^T Q_r.
+//   bwd_finalize_kernel the dgamma and dlambda sums, in a fixed order.
+// dQ and dK/dV come from separate sweeps (the dQ sweep recomputes S and dP),
+// so every gradient is written once, by one CTA, without atomics: results
+// are deterministic.
+#pragma once
+
+#include "sm103_ptx.cuh"
+
+namespace diffattn {
+
+struct BwdParams {
+    int B, H, Nq, Nk;
+    int Nq_pad;             // Nq rounded up to 128: rows of the per-row constants
+    int nchunk;             // Nq_pad / 64: row blocks of the prep kernel
+    float lambda, lambda_init, eps;
+    float scale_log2;       // log2(e) / sqrt(d)
+    float scale;            // 1 / sqrt(d)
+    const float* gamma;     // [H*dv] or null (ones)
+    const uint16_t* dy;     // bf16 [B,H,Nq,dv]
+    const float* o;         // fp32 [B,H,Nq,dv]: pre-norm forward output
+    const float* o2;        // fp32 [B,H,Nq,dv]: A2 V
+    const float* lse;       // fp32 [2,B,H,Nq]: per-map log-sum-exp (natural log)
+    uint16_t* dout;         // bf16 [B,H,Nq,dv]: gradient of the pre-norm output
+    float4* rowc;           // [B*H*Nq_pad]: (lse1 log2 e, lse2 log2 e, D1, D2); padding rows (inf, inf, 0, 0)
+    float* gpart;           // [B*H*nchunk, dv]: dgamma partial sums
+    float* lpart;           // [B*H*nchunk]: dlambda partial sums
+    uint16_t *dq1, *dq2;    // bf16 [B,H,Nq,d]
+    uint16_t *dk1, *dk2;    // bf16 [B,H,Nk,d]
+    uint16_t* dv;           // bf16 [B,H,Nk,dv]
+    float* dlambda;         // one float, or null
+    float* dgamma;          // [H*dv], or null
+};
+
+constexpr int kBwdPrepRows = 64;   // rows per prep block (8 warps x 8 rows)
+constexpr int kBwdRowPad = 128;    // Nq_pad granularity
+
+// ----------------------------------------------------------------- prep
+
+template <int DV>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
+    constexpr int CPL = DV / 32;   // channels per lane, contiguous
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const size_t bh = (size_t)b * p.H + h;
+    const size_t BH = (size_t)p.B * p.H;
+    const float kappa = 1.0f - p.lambda_init;
+    const float log2e = 1.4426950408889634f;
+    const int c0 = lane * CPL;
+    float gam[CPL], gacc[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) {
+        gam[e] = p.gamma ? p.gamma[(size_t)h * DV + c0 + e] : 1.0f;
+        gacc[e] = 0.0f;
+    }
+    float lacc = 0.0f;
+    constexpr int RPW = kBwdPrepRows / 8;
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int i = chunk * kBwdPrepRows + warp * RPW + rr;
+        float4 rc = make_float4(INFINITY, INFINITY, 0.0f, 0.0f);
+        if (i < p.Nq) {
+            const size_t row = bh * p.Nq + i;
+            float o[CPL], o2[CPL], dy[CPL];
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) {
+                o[e] = p.o[row * DV + c0 + e];
+                o2[e] = p.o2[row * DV + c0 + e];
+                dy[e] = __uint_as_float((uint32_t)p.dy[row * DV + c0 + e] << 16);
+            }
+            // GroupNorm statistics of the row (one group = this head).
+            float s = 0.0f;
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) s += o[e];
+            const float mu = warp_sum(s) * (1.0f / DV);
+            float q = 0.0f;
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) q += (o[e] - mu) * (o[e] - mu);
+            const float rstd = rsqrtf(warp_sum(q) * (1.0f / DV) + p.eps);
+            // Through the gain and scale, then the normalisation.
+            float xh[CPL], g[CPL];
+            float sg = 0.0f, sgx = 0.0f;
+#pragma unroll
+            for (int e = 0; e < CPL; ++e) {
+                xh[e] = (o[e] - mu) * rstd;
+                g[e] = kappa * gam[e] * dy[e];
+                gacc[e] += kappa * dy[e] * xh[e];
+                sg += g[e];
+                sgx += g[e] * xh[e];
+            }
+            const float mg = warp_sum(sg) * (1.0f / DV);
+            const float mgx = warp_sum(sgx) * (1.0f / DV);
+            // do, rounded to bf16 as the tile kernels' MMAs consume it; D1 and
+            // D2 use the rounded values so that sum_j dS_r,ij = 0 holds for the
+            // operand the tensor core sees.
+            // dlambda takes the unrounded do: its terms cancel to rounding
+            // level when the norm makes y insensitive to lambda.
+            float d1 = 0.0f, d2 = 0.0f, dl = 0.0f;
+            uint32_t packed[CPL / 2];
+#pragma unroll
+            for (int e = 0; e < CPL; e += 2) {
+                const float a0 = rstd * (g[e] - mg - xh[e] * mgx);
+                const float a1 = rstd * (g[e + 1] - mg - xh[e + 1] * mgx);
+                dl += a0 * o2[e] + a1 * o2[e + 1];
+                packed[e / 2] = pack_bf16x2(a0, a1);
+                const float r0 = bf16lo_to_f32(packed[e / 2]), r1 = bf16hi_to_f32(packed[e / 2]);
+                d2 += r0 * o2[e] + r1 * o2[e + 1];
+                d1 += r0 * (o[e] + p.lambda * o2[e]) + r1 * (o[e + 1] + p.lambda * o2[e + 1]);
+            }
+            if constexpr (CPL == 4) {
+                *reinterpret_cast<uint2*>(p.dout + row * DV + c0) = make_uint2(packed[0], packed[1]);
+            } else {
+                *reinterpret_cast<uint32_t*>(p.dout + row * DV + c0) = packed[0];
+            }
+            d1 = warp_sum(d1);
+            d2 = warp_sum(d2);
+            lacc -= warp_sum(dl);
+            rc = make_float4(p.lse[bh * p.Nq + i] * log2e, p.lse[(BH + bh) * p.Nq + i] * log2e, d1, d2);
+        }
+        if (lane == 0 && i < p.Nq_pad) p.rowc[bh * p.Nq_pad + i] = rc;
+    }
+    // Block sums of the dgamma and dlambda contributions, warps in order.
+    __shared__ float sg_part[8][DV];
+    __shared__ float sl_part[8];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) sg_part[warp][c0 + e] = gacc[e];
+    if (lane == 0) sl_part[warp] = lacc;
+    __syncthreads();
+    const size_t part = bh * p.nchunk + chunk;
+    for (int c = threadIdx.x; c < DV; c += blockDim.x) {
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) t += sg_part[w][c];
+        p.gpart[part * DV + c] = t;
+    }
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) t += sl_part[w];
+        p.lpart[part] = t;
+    }
+}
+
+// ----------------------------------------------------------------- finalize
+
+// Blocks 0..H-1: dgamma of head h (sum over batches and row blocks); block H:
+// dlambda.  Fixed summation order, so repeated runs agree bit for bit.
+template <int DV>
+__global__ void __launch_bounds__(256) bwd_finalize_kernel(const BwdParams p) {
+    __shared__ float red[256];
+    const int t = threadIdx.x;
+    if ((int)blockIdx.x < p.H) {
+        if (!p.dgamma) return;
+        const int h = blockIdx.x;
+        constexpr int G = 256 / DV;
+        const int c = t % DV, g = t / DV;
+        float acc = 0.0f;
+        for (int b = 0; b < p.B; ++b) {
+            const float* base = p.gpart + ((size_t)b * p.H + h) * p.nchunk * DV;
+#pragma unroll 8
+            for (int x = g; x < p.nchunk; x += G) acc += base[(size_t)x * DV + c];
+        }
+        red[t] = acc;
+        __syncthreads();
+        if (g == 0) {
+            float s = 0.0f;
+            for (int k = 0; k < G; ++k) s += red[k * DV + c];
+            p.dgamma[(size_t)h * DV + c] = s;
+        }
+    } else {
+        if (!p.dlambda) return;
+        const size_t n = (size_t)p.B * p.H * p.nchunk;
+        float acc = 0.0f;
+        for (size_t x = t; x < n; x += 256) acc += p.lpart[x];
+        red[t] = acc;
+        __syncthreads();
+        for (int s = 128; s > 0; s >>= 1) {
+            if (t < s) red[t] += red[t + s];
+            __syncthreads();
+        }
+        if (t == 0) *p.dlambda = red[0];
+    }
+}
+
+// ----------------------------------------------------------------- dQ sweep
+
+template <int D, int DV>
+struct BwdDqLayout {
+    static constexpr int BM = 128;   // query rows per CTA (MMA M)
+    static constexpr int BN = 64;    // keys per tile
+    static constexpr int KST = 3;    // K1/K2/V ring depth
+    static constexpr uint32_t Q_BYTES = BM * D * 2;
+    static constexpr uint32_t DO_BOX = BM * 128;       // one 64-column box of dO
+    static constexpr uint32_t DO_BYTES = BM * DV * 2;
+    static constexpr uint32_t K_BYTES = BN * D * 2;
+    static constexpr uint32_t V_BOX = BN * 128;
+    static constexpr uint32_t V_BYTES = BN * DV * 2;
+    static constexpr uint32_t STAGE = 2 * K_BYTES + V_BYTES;   // K1, K2, V
+    static constexpr uint32_t OFF_Q1 = 0;
+    static constexpr uint32_t OFF_Q2 = Q_BYTES;
+    static constexpr uint32_t OFF_DO = 2 * Q_BYTES;
+    static constexpr uint32_t OFF_K = OFF_DO + DO_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_K + KST * STAGE;
+    static constexpr int B_Q = 0;
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_KEMPTY = B_KFULL + KST;
+    static constexpr int B_SFULL = B_KEMPTY + KST;   // [map][buffer]
+    static constexpr int B_PFULL = B_SFULL + 4;      // [map][buffer]
+    static constexpr int B_DQFULL = B_PFULL + 4;
+    static constexpr int NBAR = B_DQFULL + 1;
+    static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
+    static constexpr uint32_t SMEM_BYTES = USED + 1024;
+    // Tensor memory: two buffers of (S1, S2, dP), 64 columns each, then the
+    // two dQ accumulators.  dS_r (bf16) is written over the first 32 columns
+    // of S_r.
+    static constexpr uint32_t TM_BUF = 192, TM_S1 = 0, TM_S2 = 64, TM_DP = 128;
+    static constexpr uint32_t TM_DQ1 = 384, TM_DQ2 = 448;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int THREADS = 320;
+    static_assert(D == 64 && DV == 128, "backward widths");
+    static_assert(SMEM_BYTES <= 227u * 1024u && SMEM_BYTES > 114u * 1024u, "one CTA per SM");
+};
+
+template <int D, int DV, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
+              const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k1,
+              const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v,
+              const BwdParams p) {
+    using L = BwdDqLayout<D, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_qt = (p.Nq + L::BM - 1) / L::BM;
+    const int qt = num_qt - 1 - (int)blockIdx.x;   // heaviest tiles first under causal masking
+    const int h = blockIdx.y, b = blockIdx.z;
+    const size_t bh = (size_t)b * p.H + h;
+    const int q0 = qt * L::BM;
+    const int diag = p.Nk - p.Nq;
+    int kv_end = p.Nk;
+    if (CAUSAL) kv_end = min(p.Nk, q0 + L::BM + diag);
+    const int n_kv = (kv_end + L::BN - 1) / L::BN;
+
+    auto bar = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)i; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::B_Q), 1);
+        for (int s = 0; s < L::KST; ++s) {
+            mbar_init(bar(L::B_KFULL + s), 1);
+            mbar_init(bar(L::B_KEMPTY + s), 1);
+        }
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(bar(L::B_SFULL + i), 1);
+            mbar_init(bar(L::B_PFULL + i), 4);
+        }
+        mbar_init(bar(L::B_DQFULL), 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_q1);
+        prefetch_tensormap(&tm_q2);
+        prefetch_tensormap(&tm_do);
+        prefetch_tensormap(&tm_k1);
+        prefetch_tensormap(&tm_k2);
+        prefetch_tensormap(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(sb + L::OFF_TMEM_SLOT, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_TMEM_SLOT);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::Q_BYTES + L::DO_BYTES);
+            tma_load_4d(sb + L::OFF_Q1, &tm_q1, bar(L::B_Q), 0, q0, h, b);
+            tma_load_4d(sb + L::OFF_Q2, &tm_q2, bar(L::B_Q), 0, q0, h, b);
+#pragma unroll
+            for (int c = 0; c < DV / 64; ++c)
+                tma_load_4d(sb + L::OFF_DO + (uint32_t)c * L::DO_BOX, &tm_do, bar(L::B_Q), c * 64, q0, h, b);
+            int issued = 0;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int ks = j % L::KST;
+                ok = mbar_wait(bar(L::B_KEMPTY + ks), ((j / L::KST) & 1) ^ 1, ERR_SITE_BWD_PRODUCER);
+                if (!ok) break;
+                const uint32_t st = sb + L::OFF_K + (uint32_t)ks * L::STAGE;
+                mbar_arrive_expect_tx(bar(L::B_KFULL + ks), L::STAGE);
+                tma_load_4d(st, &tm_k1, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
+                tma_load_4d(st + L::K_BYTES, &tm_k2, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
+#pragma unroll
+                for (int c = 0; c < DV / 64; ++c)
+                    tma_load_4d(st + 2 * L::K_BYTES + (uint32_t)c * L::V_BOX, &tm_v, bar(L::B_KFULL + ks), c * 64,
+                                j * L::BN, h, b);
+                ++issued;
+            }
+            mbar_wait(bar(L::B_Q), 0, ERR_SITE_BWD_DRAIN);
+            for (int s = 0; s < L::KST && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / L::KST) * L::KST;
+                mbar_wait(bar(L::B_KFULL + s), (last / L::KST) & 1, ERR_SITE_BWD_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(L::BM, L::BN, false);   // S, dP: K-major operands
+            constexpr uint32_t idesc_dq = idesc_bf16_f32(L::BM, D, true);       // dQ: K tile MN-major
+            bool ok = mbar_wait(bar(L::B_Q), 0, ERR_SITE_BWD_MMA);
+            tc_fence_after();
+            const uint64_t dq1 = smem_desc(sb + L::OFF_Q1, 16, 1024, SWZ_128B);
+            const uint64_t dq2 = smem_desc(sb + L::OFF_Q2, 16, 1024, SWZ_128B);
+            const uint64_t ddo = smem_desc(sb + L::OFF_DO, 16, 1024, SWZ_128B);
+            const uint64_t dk0 = smem_desc(sb + L::OFF_K, 16, 1024, SWZ_128B);                   // K1, stage 0
+            const uint64_t dkm0 = smem_desc(sb + L::OFF_K, L::K_BYTES, 1024, SWZ_128B);          // K1 as MN-major B
+            const uint64_t dv0 = smem_desc(sb + L::OFF_K + 2 * L::K_BYTES, 16, 1024, SWZ_128B);  // V, stage 0
+            constexpr uint64_t STAGE16 = L::STAGE >> 4, K2OFF = L::K_BYTES >> 4;
+            for (int j = 0; j <= n_kv && ok; ++j) {
+                if (j < n_kv) {
+                    const int ks = j % L::KST;
+                    ok = mbar_wait(bar(L::B_KFULL + ks), (j / L::KST) & 1, ERR_SITE_BWD_MMA);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t tb = tmem + (uint32_t)(j & 1) * L::TM_BUF;
+                    const uint64_t so = (uint64_t)ks * STAGE16;
+                    // dP = dO V^T: k over dv, two 64-column boxes of each operand.
+#pragma unroll
+                    for (int k = 0; k < DV / 16; ++k)
+                        mma_ss(tb + L::TM_DP, ddo + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4),
+                               dv0 + so + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4), idesc_s,
+                               k > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)
+                        mma_ss(tb + L::TM_S1, dq1 + (uint64_t)(2 * k), dk0 + so + (uint64_t)(2 * k), idesc_s,
+                               k > 0 ? 1u : 0u);
+                    mma_commit(bar(L::B_SFULL + 0 * 2 + (j & 1)));
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)
+                        mma_ss(tb + L::TM_S2, dq2 + (uint64_t)(2 * k), dk0 + so + K2OFF + (uint64_t)(2 * k), idesc_s,
+                               k > 0 ? 1u : 0u);
+                    mma_commit(bar(L::B_SFULL + 1 * 2 + (j & 1)));
+                }
+                if (j >= 1) {
+                    // dQ_r += dS_r K_r for the previous tile; dS_r (bf16) sits
+                    // in the first 32 columns of S_r, 8 columns per 16 keys.
+                    const int jp = j - 1;
+                    const int ksp = jp % L::KST;
+                    const uint32_t tb = tmem + (uint32_t)(jp & 1) * L::TM_BUF;
+                    const uint64_t so = (uint64_t)ksp * STAGE16;
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        ok = mbar_wait(bar(L::B_PFULL + r * 2 + (jp & 1)), (jp >> 1) & 1, ERR_SITE_BWD_MMA);
+                        if (!ok) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k = 0; k < L::BN / 16; ++k)
+                            mma_ts(tmem + (r ? L::TM_DQ2 : L::TM_DQ1), tb + (r ? L::TM_S2 : L::TM_S1) + 8u * k,
+                                   dkm0 + so + (r ? K2OFF : 0) + (uint64_t)(k * (16 * 128 >> 4)), idesc_dq,
+                                   (jp > 0 || k > 0) ? 1u : 0u);
+                    }
+                    if (!ok) break;
+                    mma_commit(bar(L::B_KEMPTY + ksp));
+                }
+            }
+            mma_commit(bar(L::B_DQFULL));
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ dS (warps 2-9)
+        const int r = (warp - 2) >> 2;          // map
+        const int wq = warp & 3;                // TMEM lane quarter
+        const int row = wq * 32 + lane;
+        const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+        const int qi = q0 + row;
+        const int kmax = CAUSAL ? min(qi + diag, p.Nk - 1) : p.Nk - 1;
+        const float4 rc = p.rowc[bh * p.Nq_pad + qi];
+        const float nlse = -(r ? rc.y : rc.x);
+        const float Dr = r ? rc.w : rc.z;
+        const float coef = r ? -p.lambda : 1.0f;
+        const float sl2 = p.scale_log2;
+        const uint32_t s_col = r ? L::TM_S2 : L::TM_S1;
+        bool ok = true;
+        for (int j = 0; j < n_kv; ++j) {
+            ok = mbar_wait(bar(L::B_SFULL + r * 2 + (j & 1)), (j >> 1) & 1, ERR_SITE_BWD_SOFTMAX);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t tb = tmem + t_lane + (uint32_t)(j & 1) * L::TM_BUF;
+            uint32_t sv[64], dp[64];
+            tmem_ld64(tb + s_col, sv);
+            tmem_ld64(tb + L::TM_DP, dp);
+            const int kb = j * L::BN;
+            if (kb + L::BN - 1 > kmax) {
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (kb + i > kmax) sv[i] = __float_as_uint(-INFINITY);
+            }
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) {
+                float x0, x1;
+                fma2_bcast(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), sl2, nlse);
+                const float p0 = fast_exp2(x0) * coef, p1 = fast_exp2(x1) * coef;
+                pk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - Dr), p1 * (__uint_as_float(dp[i + 1]) - Dr));
+            }
+            tmem_st32(tb + s_col, pk);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::B_PFULL + r * 2 + (j & 1)));
+        }
+        // ------------------------------------------------------------ epilogue
+        mbar_wait(bar(L::B_DQFULL), 0, ERR_SITE_BWD_EPILOGUE);
+        __syncwarp();
+        tc_fence_after();
+        uint32_t a[64];
+        tmem_ld64(tmem + t_lane + (r ? L::TM_DQ2 : L::TM_DQ1), a);
+        if (qi < p.Nq) {
+            uint4* dst = reinterpret_cast<uint4*>((r ? p.dq2 : p.dq1) + (bh * p.Nq + qi) * D);
+#pragma unroll
+            for (int i = 0; i < D / 8; ++i) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack_bf16x2(__uint_as_float(a[8 * i + 2 * e]) * p.scale,
+                                       __uint_as_float(a[8 * i + 2 * e + 1]) * p.scale);
+                dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+// ----------------------------------------------------------------- dK/dV sweep
+
+template <int D, int DV>
+struct BwdDkvLayout {
+    static constexpr int BK = 128;   // keys per CTA (MMA M)
+    static constexpr int BQ = 64;    // query rows per tile
+    static constexpr int QST = 3;    // ring depth of (Q1, Q2, dO, row constants)
+    static constexpr uint32_t K_BYTES = BK * D * 2;
+    static constexpr uint32_t V_BOX = BK * 128;
+    static constexpr uint32_t V_BYTES = BK * DV * 2;
+    static constexpr uint32_t Q_BYTES = BQ * D * 2;
+    static constexpr uint32_t DO_BOX = BQ * 128;
+    static constexpr uint32_t DO_BYTES = BQ * DV * 2;
+    static constexpr uint32_t RC_BYTES = BQ * 16;
+    static constexpr uint32_t STAGE = 2 * Q_BYTES + DO_BYTES + 1024;   // Q1, Q2, dO, row constants
+    static constexpr uint32_t ST_Q2 = Q_BYTES, ST_DO = 2 * Q_BYTES, ST_RC = 2 * Q_BYTES + DO_BYTES;
+    static constexpr uint32_t OFF_K1 = 0;
+    static constexpr uint32_t OFF_K2 = K_BYTES;
+    static constexpr uint32_t OFF_V = 2 * K_BYTES;
+    static constexpr uint32_t OFF_Q = OFF_V + V_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_Q + QST * STAGE;
+    static constexpr int B_KV = 0;
+    static constexpr int B_QFULL = 1;
+    static constexpr int B_QEMPTY = B_QFULL + QST;
+    static constexpr int B_SFULL = B_QEMPTY + QST;
+    static constexpr int B_PFULL = B_SFULL + 1;
+    static constexpr int B_DONE = B_PFULL + 1;
+    static constexpr int NBAR = B_DONE + 1;
+    static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
+    static constexpr uint32_t SMEM_BYTES = USED + 1024;
+    // Tensor memory: S1^T, S2^T, dP^T (64 columns each; dS1^T, dS2^T and
+    // (A1 - lambda A2)^T in bf16 are written over them), then the dV, dK1,
+    // dK2 accumulators.
+    static constexpr uint32_t TM_S1 = 0, TM_S2 = 64, TM_DP = 128;
+    static constexpr uint32_t TM_DV = 256, TM_DK1 = 384, TM_DK2 = 448;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int THREADS = 320;
+    static_assert(D == 64 && DV == 128, "backward widths");
+    static_assert(STAGE % 1024 == 0 && RC_BYTES <= 1024, "stage layout");
+    static_assert(SMEM_BYTES <= 227u * 1024u && SMEM_BYTES > 114u * 1024u, "one CTA per SM");
+};
+
+template <int D, int DV, bool CAUSAL>
+__global__ void __launch_bounds__(320, 1)
+bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
+               const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k1,
+               const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v,
+               const BwdParams p) {
+    using L = BwdDkvLayout<D, DV>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_addr(smem);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int kt = blockIdx.x;   // key tile 0 sees the most queries under causal masking: first
+    const int h = blockIdx.y, b = blockIdx.z;
+    const size_t bh = (size_t)b * p.H + h;
+    const int k0 = kt * L::BK;
+    const int diag = p.Nk - p.Nq;
+    // Query tiles that see at least one of this CTA's keys: key j is seen by
+    // query i iff j <= i + diag.
+    const int t0 = CAUSAL ? max(0, k0 - diag) / L::BQ : 0;
+    const int n_t = (p.Nq + L::BQ - 1) / L::BQ - t0;
+
+    auto bar = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)i; };
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::B_KV), 1);
+        for (int s = 0; s < L::QST; ++s) {
+            mbar_init(bar(L::B_QFULL + s), 1);
+            mbar_init(bar(L::B_QEMPTY + s), 1);
+        }
+        mbar_init(bar(L::B_SFULL), 1);
+        mbar_init(bar(L::B_PFULL), 8);
+        mbar_init(bar(L::B_DONE), 1);
+        fence_mbar_init();
+        prefetch_tensormap(&tm_q1);
+        prefetch_tensormap(&tm_q2);
+        prefetch_tensormap(&tm_do);
+        prefetch_tensormap(&tm_k1);
+        prefetch_tensormap(&tm_k2);
+        prefetch_tensormap(&tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(sb + L::OFF_TMEM_SLOT, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_TMEM_SLOT);
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            bool ok = true;
+            mbar_arrive_expect_tx(bar(L::B_KV), 2 * L::K_BYTES + L::V_BYTES);
+            tma_load_4d(sb + L::OFF_K1, &tm_k1, bar(L::B_KV), 0, k0, h, b);
+            tma_load_4d(sb + L::OFF_K2, &tm_k2, bar(L::B_KV), 0, k0, h, b);
+#pragma unroll
+            for (int c = 0; c < DV / 64; ++c)
+                tma_load_4d(sb + L::OFF_V + (uint32_t)c * L::V_BOX, &tm_v, bar(L::B_KV), c * 64, k0, h, b);
+            int issued = 0;
+            for (int t = 0; t < n_t && ok; ++t) {
+                const int qs = t % L::QST;
+                ok = mbar_wait(bar(L::B_QEMPTY + qs), ((t / L::QST) & 1) ^ 1, ERR_SITE_BWD_PRODUCER);
+                if (!ok) break;
+                const int i0 = (t0 + t) * L::BQ;
+                const uint32_t st = sb + L::OFF_Q + (uint32_t)qs * L::STAGE;
+                mbar_arrive_expect_tx(bar(L::B_QFULL + qs), 2 * L::Q_BYTES + L::DO_BYTES + L::RC_BYTES);
+                tma_load_4d(st, &tm_q1, bar(L::B_QFULL + qs), 0, i0, h, b);
+                tma_load_4d(st + L::ST_Q2, &tm_q2, bar(L::B_QFULL + qs), 0, i0, h, b);
+#pragma unroll
+                for (int c = 0; c < DV / 64; ++c)
+                    tma_load_4d(st + L::ST_DO + (uint32_t)c * L::DO_BOX, &tm_do, bar(L::B_QFULL + qs), c * 64, i0, h,
+                                b);
+                bulk_load(st + L::ST_RC, p.rowc + bh * p.Nq_pad + i0, L::RC_BYTES, bar(L::B_QFULL + qs));
+                ++issued;
+            }
+            mbar_wait(bar(L::B_KV), 0, ERR_SITE_BWD_DRAIN);
+            for (int s = 0; s < L::QST && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / L::QST) * L::QST;
+                mbar_wait(bar(L::B_QFULL + s), (last / L::QST) & 1, ERR_SITE_BWD_DRAIN);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_bf16_f32(L::BK, L::BQ, false);   // S^T, dP^T
+            constexpr uint32_t idesc_dv = idesc_bf16_f32(L::BK, DV, true);      // dV: dO MN-major
+            constexpr uint32_t idesc_dk = idesc_bf16_f32(L::BK, D, true);       // dK: Q MN-major
+            bool ok = mbar_wait(bar(L::B_KV), 0, ERR_SITE_BWD_MMA);
+            tc_fence_after();
+            const uint64_t dk1 = smem_desc(sb + L::OFF_K1, 16, 1024, SWZ_128B);
+            const uint64_t dk2 = smem_desc(sb + L::OFF_K2, 16, 1024, SWZ_128B);
+            const uint64_t dvv = smem_desc(sb + L::OFF_V, 16, 1024, SWZ_128B);
+            const uint64_t dq0 = smem_desc(sb + L::OFF_Q, 16, 1024, SWZ_128B);                 // Q1 (K-major), stage 0
+            const uint64_t dqm0 = smem_desc(sb + L::OFF_Q, L::Q_BYTES, 1024, SWZ_128B);        // Q1 as MN-major B
+            const uint64_t ddo0 = smem_desc(sb + L::OFF_Q + L::ST_DO, 16, 1024, SWZ_128B);     // dO (K-major)
+            const uint64_t ddom0 = smem_desc(sb + L::OFF_Q + L::ST_DO, L::DO_BOX, 1024, SWZ_128B);   // dO MN-major
+            constexpr uint64_t STAGE16 = L::STAGE >> 4, Q2OFF = L::ST_Q2 >> 4;
+            for (int t = 0; t <= n_t && ok; ++t) {
+                if (t >= 1) {
+                    // Gradients from the previous tile: A operands are the bf16
+                    // tiles the dS warps wrote over S1^T, S2^T and dP^T.  The
+                    // warps handling query columns [32 hf, 32 hf + 32) wrote
+                    // theirs at column 32 hf: 16 queries = 8 columns.
+                    const int tp = t - 1;
+                    const int qsp = tp % L::QST;
+                    const uint64_t so = (uint64_t)qsp * STAGE16;
+                    ok = mbar_wait(bar(L::B_PFULL), tp & 1, ERR_SITE_BWD_MMA);
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 0; k < L::BQ / 16; ++k) {
+                        const uint32_t acol = (uint32_t)((k >> 1) * 32 + (k & 1) * 8);
+                        const uint64_t ko = (uint64_t)(k * (16 * 128 >> 4));
+                        const uint32_t acc = (tp > 0 || k > 0) ? 1u : 0u;
+                        mma_ts(tmem + L::TM_DV, tmem + L::TM_DP + acol, ddom0 + so + ko, idesc_dv, acc);
+                        mma_ts(tmem + L::TM_DK1, tmem + L::TM_S1 + acol, dqm0 + so + ko, idesc_dk, acc);
+                        mma_ts(tmem + L::TM_DK2, tmem + L::TM_S2 + acol, dqm0 + so + Q2OFF + ko, idesc_dk, acc);
+                    }
+                    mma_commit(bar(L::B_QEMPTY + qsp));
+                }
+                if (t < n_t) {
+                    const int qs = t % L::QST;
+                    ok = mbar_wait(bar(L::B_QFULL + qs), (t / L::QST) & 1, ERR_SITE_BWD_MMA);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t so = (uint64_t)qs * STAGE16;
+                    // dP^T = V dO^T: k over dv, two 64-column boxes of each operand.
+#pragma unroll
+                    for (int k = 0; k < DV / 16; ++k)
+                        mma_ss(tmem + L::TM_DP, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
+                               ddo0 + so + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
+                               k > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)
+                        mma_ss(tmem + L::TM_S1, dk1 + (uint64_t)(2 * k), dq0 + so + (uint64_t)(2 * k), idesc_s,
+                               k > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k)
+                        mma_ss(tmem + L::TM_S2, dk2 + (uint64_t)(2 * k), dq0 + so + Q2OFF + (uint64_t)(2 * k), idesc_s,
+                               k > 0 ? 1u : 0u);
+                    mma_commit(bar(L::B_SFULL));
+                }
+            }
+            mma_commit(bar(L::B_DONE));
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ dS (warps 2-9)
+        const int hf = (warp - 2) >> 2;         // query columns [32 hf, 32 hf + 32) of each tile
+        const int wq = warp & 3;                // TMEM lane quarter
+        const int row = wq * 32 + lane;         // key row within the tile
+        const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+        const int kj = k0 + row;
+        const float sl2 = p.scale_log2;
+        const float lam = p.lambda;
+        const uint32_t cofs = (uint32_t)(32 * hf);
+        bool ok = true;
+        for (int t = 0; t < n_t; ++t) {
+            const int qs = t % L::QST;
+            ok = mbar_wait(bar(L::B_SFULL), t & 1, ERR_SITE_BWD_SOFTMAX);
+            // The row constants came in with this stage's copies: observe that
+            // barrier too (its phase cannot move on before this tile's PFULL
+            // arrival).
+            ok = ok && mbar_wait(bar(L::B_QFULL + qs), (t / L::QST) & 1, ERR_SITE_BWD_SOFTMAX);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t s1[32], s2[32], dp[32];
+            tmem_ld32(tmem + t_lane + L::TM_S1 + cofs, s1);
+            tmem_ld32(tmem + t_lane + L::TM_S2 + cofs, s2);
+            tmem_ld32(tmem + t_lane + L::TM_DP + cofs, dp);
+            const float4* rcs = reinterpret_cast<const float4*>(smem + L::OFF_Q + (uint32_t)qs * L::STAGE + L::ST_RC) +
+                                32 * hf;
+            const int qbase = (t0 + t) * L::BQ + 32 * hf;   // query of column 0
+            // Causal: key kj is hidden from query q iff kj > q + diag.
+            const bool masked = CAUSAL && (kj > qbase + diag);
+            uint32_t w1[16], w2[16], wd[16];
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float4 ra = rcs[i], rb = rcs[i + 1];
+                float p10 = fast_exp2(fmaf(__uint_as_float(s1[i]), sl2, -ra.x));
+                float p11 = fast_exp2(fmaf(__uint_as_float(s1[i + 1]), sl2, -rb.x));
+                float p20 = fast_exp2(fmaf(__uint_as_float(s2[i]), sl2, -ra.y));
+                float p21 = fast_exp2(fmaf(__uint_as_float(s2[i + 1]), sl2, -rb.y));
+                if (masked) {
+                    if (kj > qbase + i + diag) p10 = p20 = 0.0f;
+                    if (kj > qbase + i + 1 + diag) p11 = p21 = 0.0f;
+                }
+                const float d0 = __uint_as_float(dp[i]), d1 = __uint_as_float(dp[i + 1]);
+                w1[i >> 1] = pack_bf16x2(p10 * (d0 - ra.z), p11 * (d1 - rb.z));
+                w2[i >> 1] = pack_bf16x2(-lam * p20 * (d0 - ra.w), -lam * p21 * (d1 - rb.w));
+                wd[i >> 1] = pack_bf16x2(p10 - lam * p20, p11 - lam * p21);
+            }
+            tmem_st16(tmem + t_lane + L::TM_S1 + cofs, w1);
+            tmem_st16(tmem + t_lane + L::TM_S2 + cofs, w2);
+            tmem_st16(tmem + t_lane + L::TM_DP + cofs, wd);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::B_PFULL));
+        }
+        // ------------------------------------------------------------ epilogue
+        mbar_wait(bar(L::B_DONE), 0, ERR_SITE_BWD_EPILOGUE);
+        __syncwarp();
+        tc_fence_after();
+        const bool store = kj < p.Nk;
+        // dV: columns [64 hf, 64 hf + 64).
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            uint32_t a[32];
+            tmem_ld32(tmem + t_lane + L::TM_DV + 64 * hf + 32 * c, a);
+            if (store) {
+                uint4* dst = reinterpret_cast<uint4*>(p.dv + (bh * p.Nk + kj) * DV + 64 * hf + 32 * c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * i]), __uint_as_float(a[8 * i + 1])),
+                                        pack_bf16x2(__uint_as_float(a[8 * i + 2]), __uint_as_float(a[8 * i + 3])),
+                                        pack_bf16x2(__uint_as_float(a[8 * i + 4]), __uint_as_float(a[8 * i + 5])),
+                                        pack_bf16x2(__uint_as_float(a[8 * i + 6]), __uint_as_float(a[8 * i + 7])));
+            }
+        }
+        // dK1, dK2: columns [32 hf, 32 hf + 32), times 1/sqrt(d).
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            uint32_t a[32];
+            tmem_ld32(tmem + t_lane + (r ? L::TM_DK2 : L::TM_DK1) + 32 * hf, a);
+            if (store) {
+                uint4* dst = reinterpret_cast<uint4*>((r ? p.dk2 : p.dk1) + (bh * p.Nk + kj) * D + 32 * hf);
+                const float s = p.scale;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(
+                        pack_bf16x2(__uint_as_float(a[8 * i]) * s, __uint_as_float(a[8 * i + 1]) * s),
+                        pack_bf16x2(__uint_as_float(a[8 * i + 2]) * s, __uint_as_float(a[8 * i + 3]) * s),
+                        pack_bf16x2(__uint_as_float(a[8 * i + 4]) * s, __uint_as_float(a[8 * i + 5]) * s),
+                        pack_bf16x2(__uint_as_float(a[8 * i + 6]) * s, __uint_as_float(a[8 * i + 7]) * s));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+}  // namespace diffattn

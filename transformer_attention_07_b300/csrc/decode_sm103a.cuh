@@ -90,12 +90,6 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
 // Dot product of a bf16 key row held in swizzled shared memory with q (fp32
 // registers).  Row r of the tile starts at r*2D bytes; the 16-byte chunk c of
 // the row sits at chunk position c ^ ((row byte offset >> 7) & (span/16 - 1)).

@@ -34,6 +34,7 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, int s
 
 }  // namespace diffattn
 
+#include "backward_sm103a.cuh"
 #include "decode_sm103a.cuh"
 #include "prefill_sm103a.cuh"
 #include "standard_attn_sm103a.cuh"
@@ -107,6 +108,8 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     p.gamma = a.gamma;
     p.out = static_cast<uint16_t*>(a.out);
     p.o_prenorm = a.o_prenorm;
+    p.o2 = a.o2;
+    p.lse = a.lse;
     auto kern = prefill_kernel<D, DV, CAUSAL>;
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
                  "prefill: set shared memory"))
@@ -121,6 +124,107 @@ int launch_prefill(const PrefillArgs& a, cudaStream_t st) {
         return a.causal ? launch_prefill_t<64, 128, true>(a, st) : launch_prefill_t<64, 128, false>(a, st);
     if (a.d == 32 && a.dv == 64)
         return a.causal ? launch_prefill_t<32, 64, true>(a, st) : launch_prefill_t<32, 64, false>(a, st);
+    return LAUNCH_ERR_UNSUPPORTED;
+}
+
+// ----------------------------------------------------------------- backward
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int dv) {
+    BwdWorkspace w;
+    const size_t BH = (size_t)B * H;
+    w.Nq_pad = (Nq + kBwdRowPad - 1) / kBwdRowPad * kBwdRowPad;
+    w.nchunk = w.Nq_pad / kBwdPrepRows;
+    w.off_do = 0;
+    w.off_rowc = align256(BH * Nq * dv * 2);
+    w.off_gpart = w.off_rowc + align256(BH * w.Nq_pad * 16);
+    w.off_lpart = w.off_gpart + align256(BH * w.nchunk * dv * 4);
+    w.total = w.off_lpart + align256(BH * w.nchunk * 4);
+    return w;
+}
+
+template <int D, int DV, bool CAUSAL>
+static int launch_backward_t(const BwdArgs& a, cudaStream_t st) {
+    using LQ = BwdDqLayout<D, DV>;
+    using LK = BwdDkvLayout<D, DV>;
+    const BwdWorkspace w = bwd_workspace_layout(a.B, a.H, a.Nq, DV);
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    BwdParams p;
+    p.B = a.B;
+    p.H = a.H;
+    p.Nq = a.Nq;
+    p.Nk = a.Nk;
+    p.Nq_pad = w.Nq_pad;
+    p.nchunk = w.nchunk;
+    p.lambda = a.lambda;
+    p.lambda_init = a.lambda_init;
+    p.eps = a.eps;
+    p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+    p.scale = (float)(1.0 / std::sqrt((double)D));
+    p.gamma = a.gamma;
+    p.dy = static_cast<const uint16_t*>(a.dy);
+    p.o = a.o;
+    p.o2 = a.o2;
+    p.lse = a.lse;
+    p.dout = reinterpret_cast<uint16_t*>(ws + w.off_do);
+    p.rowc = reinterpret_cast<float4*>(ws + w.off_rowc);
+    p.gpart = reinterpret_cast<float*>(ws + w.off_gpart);
+    p.lpart = reinterpret_cast<float*>(ws + w.off_lpart);
+    p.dq1 = static_cast<uint16_t*>(a.dq1);
+    p.dq2 = static_cast<uint16_t*>(a.dq2);
+    p.dk1 = static_cast<uint16_t*>(a.dk1);
+    p.dk2 = static_cast<uint16_t*>(a.dk2);
+    p.dv = static_cast<uint16_t*>(a.dv_grad);
+    p.dlambda = a.dlambda;
+    p.dgamma = a.dgamma;
+
+    bwd_prep_kernel<DV><<<dim3(w.nchunk, a.H, a.B), 256, 0, st>>>(p);
+    if (!cuda_ok(cudaGetLastError(), "backward: prep launch")) return LAUNCH_ERR_CUDA;
+
+    CUtensorMap q1a, q2a, doa, k1a, k2a, va;   // dQ sweep: 128-row Q/dO boxes, 64-row K/V boxes
+    CUtensorMap q1b, q2b, dob, k1b, k2b, vb;   // dK/dV sweep: 64-row Q/dO boxes, 128-row K/V boxes
+    const auto S = CU_TENSOR_MAP_SWIZZLE_128B;
+    if (!make_map_bhnd(&q1a, a.q1, a.B, a.H, a.Nq, D, 64, LQ::BM, S) ||
+        !make_map_bhnd(&q2a, a.q2, a.B, a.H, a.Nq, D, 64, LQ::BM, S) ||
+        !make_map_bhnd(&doa, p.dout, a.B, a.H, a.Nq, DV, 64, LQ::BM, S) ||
+        !make_map_bhnd(&k1a, a.k1, a.B, a.H, a.Nk, D, 64, LQ::BN, S) ||
+        !make_map_bhnd(&k2a, a.k2, a.B, a.H, a.Nk, D, 64, LQ::BN, S) ||
+        !make_map_bhnd(&va, a.v, a.B, a.H, a.Nk, DV, 64, LQ::BN, S) ||
+        !make_map_bhnd(&q1b, a.q1, a.B, a.H, a.Nq, D, 64, LK::BQ, S) ||
+        !make_map_bhnd(&q2b, a.q2, a.B, a.H, a.Nq, D, 64, LK::BQ, S) ||
+        !make_map_bhnd(&dob, p.dout, a.B, a.H, a.Nq, DV, 64, LK::BQ, S) ||
+        !make_map_bhnd(&k1b, a.k1, a.B, a.H, a.Nk, D, 64, LK::BK, S) ||
+        !make_map_bhnd(&k2b, a.k2, a.B, a.H, a.Nk, D, 64, LK::BK, S) ||
+        !make_map_bhnd(&vb, a.v, a.B, a.H, a.Nk, DV, 64, LK::BK, S))
+        return LAUNCH_ERR_CUDA;
+
+    auto kq = bwd_dq_kernel<D, DV, CAUSAL>;
+    if (!cuda_ok(cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LQ::SMEM_BYTES),
+                 "backward: dq shared memory"))
+        return LAUNCH_ERR_CUDA;
+    kq<<<dim3((a.Nq + LQ::BM - 1) / LQ::BM, a.H, a.B), LQ::THREADS, LQ::SMEM_BYTES, st>>>(q1a, q2a, doa, k1a, k2a,
+                                                                                          va, p);
+    if (!cuda_ok(cudaGetLastError(), "backward: dq launch")) return LAUNCH_ERR_CUDA;
+
+    auto kk = bwd_dkv_kernel<D, DV, CAUSAL>;
+    if (!cuda_ok(cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)LK::SMEM_BYTES),
+                 "backward: dkv shared memory"))
+        return LAUNCH_ERR_CUDA;
+    kk<<<dim3((a.Nk + LK::BK - 1) / LK::BK, a.H, a.B), LK::THREADS, LK::SMEM_BYTES, st>>>(q1b, q2b, dob, k1b, k2b,
+                                                                                          vb, p);
+    if (!cuda_ok(cudaGetLastError(), "backward: dkv launch")) return LAUNCH_ERR_CUDA;
+
+    if (a.dgamma || a.dlambda) {
+        bwd_finalize_kernel<DV><<<a.H + 1, 256, 0, st>>>(p);
+        if (!cuda_ok(cudaGetLastError(), "backward: finalize launch")) return LAUNCH_ERR_CUDA;
+    }
+    return LAUNCH_OK;
+}
+
+int launch_backward(const BwdArgs& a, cudaStream_t st) {
+    if (a.d == 64 && a.dv == 128)
+        return a.causal ? launch_backward_t<64, 128, true>(a, st) : launch_backward_t<64, 128, false>(a, st);
     return LAUNCH_ERR_UNSUPPORTED;
 }
 

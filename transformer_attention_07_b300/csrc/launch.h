@@ -21,6 +21,8 @@ struct PrefillArgs {
     const float* gamma;
     void* out;
     float* o_prenorm;
+    float* o2;    // training outputs (null for inference)
+    float* lse;
 };
 
 struct DecodeArgs {
@@ -49,7 +51,27 @@ struct StandardArgs {
     float* out_f32;
 };
 
+struct BwdArgs {
+    const void *q1, *k1, *q2, *k2, *v, *dy;
+    const float *o, *o2, *lse;
+    float lambda, lambda_init, eps;
+    int causal, B, H, Nq, Nk, d, dv;
+    const float* gamma;
+    void *dq1, *dk1, *dq2, *dk2, *dv_grad;
+    float *dlambda, *dgamma;
+    void* ws;   // >= bwd_workspace_bytes(B, H, Nq, dv), 256-byte aligned
+};
+
+// Workspace of the backward pass: do (bf16), the per-row constants, and the
+// dgamma / dlambda partial sums, each 256-byte aligned.
+struct BwdWorkspace {
+    size_t off_do, off_rowc, off_gpart, off_lpart, total;
+    int Nq_pad, nchunk;
+};
+BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int dv);
+
 int launch_prefill(const PrefillArgs& a, cudaStream_t st);
+int launch_backward(const BwdArgs& a, cudaStream_t st);
 int launch_standard(const StandardArgs& a, cudaStream_t st);
 int launch_decode(const DecodeArgs& a, cudaStream_t st);
 int read_and_clear_device_error(cudaStream_t st, int* value);

@@ -27,7 +27,9 @@
 //                2^8 (values stay bounded by 2^8 in between).
 //   epilogue     both softmax groups: o = O1/l1 - lambda O2/l2 per row, the
 //                GroupNorm statistics over dv, gain, (1 - lambda_init), bf16
-//                store (and the optional fp32 pre-norm copy).
+//                store (and the optional fp32 pre-norm copy; for training,
+//                also each map's log-sum-exp and A2 V, which the backward
+//                pass reads).
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   [0,128) S1 (P1 aliases its first 64 columns)   [128,256) S2 / P2
 //   [256,256+dv) O1                                [256+dv,256+2dv) O2
@@ -44,6 +46,8 @@ struct PrefillParams {
     const float* gamma;     // [H*dv] or null
     uint16_t* out;          // bf16 [B,H,Nq,dv]
     float* o_prenorm;       // fp32 [B,H,Nq,dv] or null
+    float* o2;              // fp32 [B,H,Nq,dv] or null: A2 V (the second map's normalised output)
+    float* lse;             // fp32 [2,B,H,Nq] or null: log sum_j exp(s_r,ij), natural log, per map
 };
 
 template <int D, int DV>
@@ -357,6 +361,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         const float inv2 = p.lambda / epi[L::BM + row];
         constexpr int HALF = DV / 2;
         const int c0 = r * HALF;
+        const size_t rowoff = (((size_t)b * p.H + h) * p.Nq + qi) * DV + c0;
+        // Training outputs for the backward pass: each map's log-sum-exp of
+        // the scaled logits (natural log; m is in log2 units) and A2 V.
+        if (p.lse != nullptr && qi < p.Nq)
+            p.lse[((size_t)r * p.B * p.H + (size_t)b * p.H + h) * p.Nq + qi] = (m + log2f(l)) * 0.6931471805599453f;
+        float* o2row = (p.o2 != nullptr && qi < p.Nq) ? p.o2 + rowoff : nullptr;
+        const float inv2n = 1.0f / epi[L::BM + row];
         float o[HALF];
 #pragma unroll
         for (int c = 0; c < HALF / 32; ++c) {
@@ -368,6 +379,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 // Both products rounded before the subtraction (no FMA
                 // contraction), so identical maps with lambda = 1 cancel to 0.
                 o[32 * c + i] = __fmul_rn(__uint_as_float(a[i]), inv1) - __fmul_rn(__uint_as_float(bb[i]), inv2);
+            if (o2row) {
+                float4* dst = reinterpret_cast<float4*>(o2row + 32 * c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(__uint_as_float(bb[4 * i]) * inv2n, __uint_as_float(bb[4 * i + 1]) * inv2n,
+                                         __uint_as_float(bb[4 * i + 2]) * inv2n, __uint_as_float(bb[4 * i + 3]) * inv2n);
+            }
         }
         float sum = 0.f;
 #pragma unroll
@@ -383,7 +401,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         const float var = (epi[4 * L::BM + row] + epi[5 * L::BM + row]) * (1.0f / DV);
         const float sc = (1.0f - p.lambda_init) * rsqrtf(var + p.eps);
         if (qi < p.Nq) {
-            const size_t rowoff = (((size_t)b * p.H + h) * p.Nq + qi) * DV + c0;
             if (p.o_prenorm) {
                 float4* dst = reinterpret_cast<float4*>(p.o_prenorm + rowoff);
 #pragma unroll

@@ -25,6 +25,11 @@ enum : int {
     ERR_SITE_DECODE_PRODUCER = 0x201,
     ERR_SITE_DECODE_CONSUMER = 0x202,
     ERR_SITE_DECODE_DRAIN = 0x203,
+    ERR_SITE_BWD_PRODUCER = 0x401,
+    ERR_SITE_BWD_MMA = 0x402,
+    ERR_SITE_BWD_SOFTMAX = 0x403,
+    ERR_SITE_BWD_EPILOGUE = 0x404,
+    ERR_SITE_BWD_DRAIN = 0x405,
     ERR_DECODE_BAD_PAGE = 0x301,      // a block-table entry outside [0, num_pages): clamped, not read
     ERR_DECODE_BAD_LENGTH = 0x302,    // a sequence length outside [1, max_pages * page_size): clamped
 };
@@ -227,6 +232,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+// Store 16 consecutive 32-bit columns of this thread's lane (not waited on).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+        " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 #define DA_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), "=r"(r[i + 5]), \
@@ -343,6 +358,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t packed) { return __uint_as_float(packed << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
+
+// Sum over the 32 lanes of a warp (every lane receives the total).
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
 
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -1,4 +1,4 @@
-"""Seeded synthetic inputs for the differential-attention forward.
+"""Seeded synthetic inputs for the differential-attention forward and backward.
 
 This module only draws numbers: it holds none of the method's arithmetic, so
 the tests, the benchmark and the oracle-side checks can all take their inputs
@@ -8,7 +8,8 @@ llmbytes.dev "The Mathematical Flaw in Standard Softmax Attention" and
 "Multi-Needle Retrieval at 64K Context"); no dataset is involved.
 
 Draw order is Q1, K1, Q2, K2, V, gamma, from one ``torch.Generator`` seeded
-per workload, in fp32, then rounded to bf16 (nearest even).
+per workload, in fp32, then rounded to bf16 (nearest even).  The upstream
+gradient of the backward pass (``make_dy``) is N(0, 1) from its own seed.
 """
 from __future__ import annotations
 
@@ -49,6 +50,13 @@ class Workload:
     def flops(self) -> int:
         """Algorithmic flops: 2 QK^T (2d each) + 2 PV (2dv each) per pair."""
         return 4 * (self.d + self.dv) * self.pairs
+
+    @property
+    def bwd_flops(self) -> int:
+        """Algorithmic flops of the backward pass per pair: S1, S2 recomputed
+        (2d each), dP = do V^T (2dv), dV (2dv), dK1, dK2 (2d each), dQ1, dQ2
+        (2d each)."""
+        return (12 * self.d + 4 * self.dv) * self.pairs
 
     @property
     def kv_bytes(self) -> int:
@@ -164,3 +172,14 @@ def sample_rows(N: int, seed: int, n_random: int = 384, edge: int = 64) -> list[
     if N > 2 * edge:
         rows |= set(torch.randint(edge, N - edge, (n_random,), generator=g).tolist())
     return sorted(rows)
+
+
+def make_dy(w: Workload, device="cuda", seed=None):
+    """Upstream gradient dL/dy for the backward pass: N(0, 1), bf16, [B,H,Nq,dv]."""
+    g = torch.Generator(device=device)
+    g.manual_seed((w.seed if seed is None else seed) + 500)
+    dy = torch.empty((w.B, w.H, w.Nq, w.dv), dtype=torch.bfloat16, device=device)
+    for b in range(w.B):
+        for h in range(w.H):
+            dy[b, h].copy_(torch.randn((w.Nq, w.dv), generator=g, device=device))
+    return dy

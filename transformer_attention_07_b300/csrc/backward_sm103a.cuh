@@ -495,17 +495,19 @@ struct BwdDkvLayout {
     static constexpr int B_KV = 0;
     static constexpr int B_QFULL = 1;
     static constexpr int B_QEMPTY = B_QFULL + QST;
-    static constexpr int B_SFULL = B_QEMPTY + QST;
-    static constexpr int B_PFULL = B_SFULL + 1;
-    static constexpr int B_DONE = B_PFULL + 1;
+    static constexpr int B_SFULL = B_QEMPTY + QST;   // [half]
+    static constexpr int B_PFULL = B_SFULL + 2;      // [half]
+    static constexpr int B_DONE = B_PFULL + 2;
     static constexpr int NBAR = B_DONE + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
     static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
     static constexpr uint32_t SMEM_BYTES = USED + 1024;
-    // Tensor memory: S1^T, S2^T, dP^T (64 columns each; dS1^T, dS2^T and
-    // (A1 - lambda A2)^T in bf16 are written over them), then the dV, dK1,
-    // dK2 accumulators.
-    static constexpr uint32_t TM_S1 = 0, TM_S2 = 64, TM_DP = 128;
+    // Tensor memory: for each half of the query tile (32 queries), S1^T,
+    // S2^T, dP^T (32 columns each; dS1^T, dS2^T and (A1 - lambda A2)^T in
+    // bf16 are written over their first 16), then the dV, dK1, dK2
+    // accumulators.
+    static constexpr int HQ = BQ / 2;                  // queries per half
+    static constexpr uint32_t TM_HALF = 96, TM_S1 = 0, TM_S2 = 32, TM_DP = 64;
     static constexpr uint32_t TM_DV = 256, TM_DK1 = 384, TM_DK2 = 448;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 320;
@@ -544,8 +546,10 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             mbar_init(bar(L::B_QFULL + s), 1);
             mbar_init(bar(L::B_QEMPTY + s), 1);
         }
-        mbar_init(bar(L::B_SFULL), 1);
-        mbar_init(bar(L::B_PFULL), 8);
+        for (int hh = 0; hh < 2; ++hh) {
+            mbar_init(bar(L::B_SFULL + hh), 1);
+            mbar_init(bar(L::B_PFULL + hh), 4);
+        }
         mbar_init(bar(L::B_DONE), 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_q1);
@@ -601,7 +605,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(L::BK, L::BQ, false);   // S^T, dP^T
+            constexpr uint32_t idesc_s = idesc_bf16_f32(L::BK, L::HQ, false);   // S^T, dP^T of one half
             constexpr uint32_t idesc_dv = idesc_bf16_f32(L::BK, DV, true);      // dV: dO MN-major
             constexpr uint32_t idesc_dk = idesc_bf16_f32(L::BK, D, true);       // dK: Q MN-major
             bool ok = mbar_wait(bar(L::B_KV), 0, ERR_SITE_BWD_MMA);
@@ -614,50 +618,56 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             const uint64_t ddo0 = smem_desc(sb + L::OFF_Q + L::ST_DO, 16, 1024, SWZ_128B);     // dO (K-major)
             const uint64_t ddom0 = smem_desc(sb + L::OFF_Q + L::ST_DO, L::DO_BOX, 1024, SWZ_128B);   // dO MN-major
             constexpr uint64_t STAGE16 = L::STAGE >> 4, Q2OFF = L::ST_Q2 >> 4;
+            constexpr uint64_t HALF16 = (L::HQ * 128) >> 4;   // 32 rows of a 128-byte-wide tile
+            // The two halves of each query tile alternate: while the dS warps
+            // of one half work, the tensor core runs the other half's
+            // gradients and next scores.
             for (int t = 0; t <= n_t && ok; ++t) {
-                if (t >= 1) {
-                    // Gradients from the previous tile: A operands are the bf16
-                    // tiles the dS warps wrote over S1^T, S2^T and dP^T.  The
-                    // warps handling query columns [32 hf, 32 hf + 32) wrote
-                    // theirs at column 32 hf: 16 queries = 8 columns.
-                    const int tp = t - 1;
-                    const int qsp = tp % L::QST;
-                    const uint64_t so = (uint64_t)qsp * STAGE16;
-                    ok = mbar_wait(bar(L::B_PFULL), tp & 1, ERR_SITE_BWD_MMA);
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll
-                    for (int k = 0; k < L::BQ / 16; ++k) {
-                        const uint32_t acol = (uint32_t)((k >> 1) * 32 + (k & 1) * 8);
-                        const uint64_t ko = (uint64_t)(k * (16 * 128 >> 4));
-                        const uint32_t acc = (tp > 0 || k > 0) ? 1u : 0u;
-                        mma_ts(tmem + L::TM_DV, tmem + L::TM_DP + acol, ddom0 + so + ko, idesc_dv, acc);
-                        mma_ts(tmem + L::TM_DK1, tmem + L::TM_S1 + acol, dqm0 + so + ko, idesc_dk, acc);
-                        mma_ts(tmem + L::TM_DK2, tmem + L::TM_S2 + acol, dqm0 + so + Q2OFF + ko, idesc_dk, acc);
-                    }
-                    mma_commit(bar(L::B_QEMPTY + qsp));
-                }
+                const int qs = t % L::QST;
                 if (t < n_t) {
-                    const int qs = t % L::QST;
                     ok = mbar_wait(bar(L::B_QFULL + qs), (t / L::QST) & 1, ERR_SITE_BWD_MMA);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint64_t so = (uint64_t)qs * STAGE16;
-                    // dP^T = V dO^T: k over dv, two 64-column boxes of each operand.
+                }
 #pragma unroll
-                    for (int k = 0; k < DV / 16; ++k)
-                        mma_ss(tmem + L::TM_DP, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
-                               ddo0 + so + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
-                               k > 0 ? 1u : 0u);
+                for (int hh = 0; hh < 2; ++hh) {
+                    const uint32_t th = tmem + (uint32_t)hh * L::TM_HALF;
+                    if (t >= 1) {
+                        // Gradients of the previous tile's half hh: A operands
+                        // are the bf16 tiles the dS warps wrote over its scores.
+                        const int tp = t - 1;
+                        const uint64_t so = (uint64_t)(tp % L::QST) * STAGE16 + (uint64_t)hh * HALF16;
+                        ok = mbar_wait(bar(L::B_PFULL + hh), tp & 1, ERR_SITE_BWD_MMA);
+                        if (!ok) break;
+                        tc_fence_after();
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k)
-                        mma_ss(tmem + L::TM_S1, dk1 + (uint64_t)(2 * k), dq0 + so + (uint64_t)(2 * k), idesc_s,
-                               k > 0 ? 1u : 0u);
+                        for (int k = 0; k < L::HQ / 16; ++k) {
+                            const uint64_t ko = (uint64_t)(k * (16 * 128 >> 4));
+                            const uint32_t acc = (tp > 0 || hh > 0 || k > 0) ? 1u : 0u;
+                            mma_ts(tmem + L::TM_DV, th + L::TM_DP + 8u * k, ddom0 + so + ko, idesc_dv, acc);
+                            mma_ts(tmem + L::TM_DK1, th + L::TM_S1 + 8u * k, dqm0 + so + ko, idesc_dk, acc);
+                            mma_ts(tmem + L::TM_DK2, th + L::TM_S2 + 8u * k, dqm0 + so + Q2OFF + ko, idesc_dk, acc);
+                        }
+                        if (hh == 1) mma_commit(bar(L::B_QEMPTY + tp % L::QST));
+                    }
+                    if (t < n_t) {
+                        const uint64_t so = (uint64_t)qs * STAGE16 + (uint64_t)hh * HALF16;
+                        // dP^T = V dO^T: k over dv, two 64-column boxes of each operand.
 #pragma unroll
-                    for (int k = 0; k < D / 16; ++k)
-                        mma_ss(tmem + L::TM_S2, dk2 + (uint64_t)(2 * k), dq0 + so + Q2OFF + (uint64_t)(2 * k), idesc_s,
-                               k > 0 ? 1u : 0u);
-                    mma_commit(bar(L::B_SFULL));
+                        for (int k = 0; k < DV / 16; ++k)
+                            mma_ss(th + L::TM_DP, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
+                                   ddo0 + so + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
+                                   k > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k)
+                            mma_ss(th + L::TM_S1, dk1 + (uint64_t)(2 * k), dq0 + so + (uint64_t)(2 * k), idesc_s,
+                                   k > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k)
+                            mma_ss(th + L::TM_S2, dk2 + (uint64_t)(2 * k), dq0 + so + Q2OFF + (uint64_t)(2 * k),
+                                   idesc_s, k > 0 ? 1u : 0u);
+                        mma_commit(bar(L::B_SFULL + hh));
+                    }
                 }
             }
             mma_commit(bar(L::B_DONE));
@@ -665,32 +675,32 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         __syncwarp();
     } else {
         // ------------------------------------------------------------ dS (warps 2-9)
-        const int hf = (warp - 2) >> 2;         // query columns [32 hf, 32 hf + 32) of each tile
+        const int hf = (warp - 2) >> 2;         // half: query columns [32 hf, 32 hf + 32) of each tile
         const int wq = warp & 3;                // TMEM lane quarter
         const int row = wq * 32 + lane;         // key row within the tile
         const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
+        const uint32_t th = tmem + t_lane + (uint32_t)hf * L::TM_HALF;
         const int kj = k0 + row;
         const float sl2 = p.scale_log2;
         const float lam = p.lambda;
-        const uint32_t cofs = (uint32_t)(32 * hf);
         bool ok = true;
         for (int t = 0; t < n_t; ++t) {
             const int qs = t % L::QST;
-            ok = mbar_wait(bar(L::B_SFULL), t & 1, ERR_SITE_BWD_SOFTMAX);
+            ok = mbar_wait(bar(L::B_SFULL + hf), t & 1, ERR_SITE_BWD_SOFTMAX);
             // The row constants came in with this stage's copies: observe that
             // barrier too (its phase cannot move on before this tile's PFULL
-            // arrival).
+            // arrivals).
             ok = ok && mbar_wait(bar(L::B_QFULL + qs), (t / L::QST) & 1, ERR_SITE_BWD_SOFTMAX);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             uint32_t s1[32], s2[32], dp[32];
-            tmem_ld32(tmem + t_lane + L::TM_S1 + cofs, s1);
-            tmem_ld32(tmem + t_lane + L::TM_S2 + cofs, s2);
-            tmem_ld32(tmem + t_lane + L::TM_DP + cofs, dp);
+            tmem_ld32(th + L::TM_S1, s1);
+            tmem_ld32(th + L::TM_S2, s2);
+            tmem_ld32(th + L::TM_DP, dp);
             const float4* rcs = reinterpret_cast<const float4*>(smem + L::OFF_Q + (uint32_t)qs * L::STAGE + L::ST_RC) +
-                                32 * hf;
-            const int qbase = (t0 + t) * L::BQ + 32 * hf;   // query of column 0
+                                L::HQ * hf;
+            const int qbase = (t0 + t) * L::BQ + L::HQ * hf;   // query of column 0
             // Causal: key kj is hidden from query q iff kj > q + diag.
             const bool masked = CAUSAL && (kj > qbase + diag);
             uint32_t w1[16], w2[16], wd[16];
@@ -710,13 +720,13 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 w2[i >> 1] = pack_bf16x2(-lam * p20 * (d0 - ra.w), -lam * p21 * (d1 - rb.w));
                 wd[i >> 1] = pack_bf16x2(p10 - lam * p20, p11 - lam * p21);
             }
-            tmem_st16(tmem + t_lane + L::TM_S1 + cofs, w1);
-            tmem_st16(tmem + t_lane + L::TM_S2 + cofs, w2);
-            tmem_st16(tmem + t_lane + L::TM_DP + cofs, wd);
+            tmem_st16(th + L::TM_S1, w1);
+            tmem_st16(th + L::TM_S2, w2);
+            tmem_st16(th + L::TM_DP, wd);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::B_PFULL));
+            if (lane == 0) mbar_arrive(bar(L::B_PFULL + hf));
         }
         // ------------------------------------------------------------ epilogue
         mbar_wait(bar(L::B_DONE), 0, ERR_SITE_BWD_EPILOGUE);

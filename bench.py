@@ -275,6 +275,40 @@ def paged_decode_throughput(dev, reps=10):
     return res
 
 
+def fp8_throughput(dev, w, inp, reps=10):
+    """The prefill with fp8 (e4m3) Q/K (per-head scales amax/448) against the
+    bf16 prefill on the same workload.  TFLOP/s counts the same algorithmic
+    flops as the bf16 path (4(d + dv) per pair); Q K^T runs at 8 bits."""
+    import torch
+    import transformer_attention_07_b300 as da
+    stream = torch.cuda.current_stream(dev)
+    q8, sc = {}, []
+    for name in ("q1", "k1", "q2", "k2"):
+        x = inp[name].float()
+        s = (x.abs().amax(dim=(0, 2, 3)).clamp_min(1e-6) / 448.0).float()
+        q8[name] = (x / s[None, :, None, None]).to(torch.float8_e4m3fn)
+        sc.append(s)
+        del x
+    scale = torch.stack(sc).contiguous().view(-1)
+    out = torch.empty((w.B, w.H, w.Nq, w.dv), dtype=torch.bfloat16, device=dev)
+    run = lambda: da.fwd_fp8(q8["q1"], q8["k1"], q8["q2"], q8["k2"], inp["v"], scale, w.lam, w.lam_init,
+                             causal=w.causal, gamma=inp["gamma"], eps=w.eps, out=out, stream=stream)
+    for _ in range(3):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        run()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if da.last_device_error() != 0:
+        raise RuntimeError("device-side error in the fp8 prefill")
+    ms = e0.elapsed_time(e1) / reps
+    del q8, out
+    return {"workload": w.name, "ms": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12,
+            "note": "Q/K e4m3 with per-head scales; QK^T on the 8-bit tensor core, P V in bf16"}
+
+
 def backward_throughput(dev, w, inp, reps=3):
     """Backward pass (prep, dQ sweep, dK/dV sweep, finalize) on workload w,
     after one training forward.  Algorithmic flops per pair 12d + 4dv (S1,
@@ -462,6 +496,8 @@ def run_cuda(args, world, rank, local):
         torch.cuda.empty_cache()
         line["decode_paged"] = paged_decode_throughput(dev)
         line["backward"] = backward_throughput(dev, wp, pin)
+        line["fp8_qk"] = fp8_throughput(dev, wp, pin)
+        line["fp8_qk"]["vs_bf16"] = line["prefill_ms"] / line["fp8_qk"]["ms"] - 1.0
     if do_pre and not args.no_cpu_baseline:
         cpu = [pin[k].cpu() for k in names]
         rows = sample_rows_uniform(wp.Nq, args.cpu_rows, 4242)

@@ -82,6 +82,24 @@ int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* 
                     const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream);
 
 /*
+ * Prefill forward with 8-bit queries and keys.  The pages link differential
+ * attention to low-bit quantisation through its smaller activation outliers
+ * (llmbytes.dev, "Quantization Friendliness").  Here q1, k1, q2, k2 are
+ * stored as fp8 e4m3 bytes [B,H,N,d] (16-byte aligned), and each
+ * (tensor, head) has a dequantisation scale:
+ *   qk_scale    [4*H] fp32, device: rows sq1, sk1, sq2, sk2, each H long,
+ *               so q_r = sq_r[h] * q8_r and k_r = sk_r[h] * k8_r
+ * The logits are s_r = sq_r[h] sk_r[h] (q8_r . k8_r) / sqrt(d), computed by
+ * the 8-bit tensor-core product with fp32 accumulation.  V, P, the output
+ * and everything after the scores are as in diffattn_fwd_ex.  The scales are
+ * read on the device, so the host cannot check them; they must be finite.
+ */
+int diffattn_fwd_fp8(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                     const float* qk_scale, float lambda, float lambda_init, int causal,
+                     int B, int H, int Nq, int Nk, int d, int dv,
+                     const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream);
+
+/*
  * Training forward: diffattn_fwd_ex plus what the backward pass reads.
  *   o_prenorm   [B,H,Nq,dv] fp32, required: (A1 - lambda A2) V
  *   o2          [B,H,Nq,dv] fp32, required, 16-byte aligned: A2 V

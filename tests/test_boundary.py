@@ -31,7 +31,7 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "diffattn_fwd", "diffattn_fwd_ex", "diffattn_fwd_train", "diffattn_bwd_workspace_bytes", "diffattn_bwd",
+        "diffattn_fwd", "diffattn_fwd_ex", "diffattn_fwd_fp8", "diffattn_fwd_train", "diffattn_bwd_workspace_bytes", "diffattn_bwd",
         "diffattn_decode_workspace_bytes", "diffattn_decode",
         "diffattn_decode_noalloc", "diffattn_decode_paged", "diffattn_standard_fwd", "diffattn_status_string",
         "diffattn_last_device_error"])
@@ -76,6 +76,18 @@ def test_fwd_empty_problems_return_ok_without_launch(lib):
     assert fwd(lib, H=0) == OK
     assert fwd(lib, Nq=0) == OK
     assert fwd(lib, Nq=0, causal=1) == OK
+
+
+def test_fwd_fp8_validation(lib):
+    f8 = lambda q=FAKE, sc=FAKE, d=64, dv=128, B=1, causal=0, Nq=4: lib.diffattn_fwd_fp8(
+        q, q, q, q, FAKE, sc, 0.5, 0.8, causal, B, 1, Nq, 4, d, dv, None, 1e-5, FAKE, None, None)
+    assert f8(sc=None) == INVALID
+    assert f8(q=None) == INVALID
+    assert f8(sc=ctypes.c_void_p(0x10002)) == INVALID
+    assert f8(q=MISALIGNED) == INVALID
+    assert f8(causal=1, Nq=5) == INVALID
+    assert f8(d=64, dv=64) == UNSUPPORTED
+    assert f8(B=0) == OK
 
 
 def test_fwd_train_validation(lib):

@@ -18,7 +18,7 @@ import ctypes
 import os
 
 __all__ = [
-    "fwd", "fwd_train", "bwd", "bwd_workspace_bytes", "standard_fwd", "decode", "decode_paged",
+    "fwd", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes", "standard_fwd", "decode", "decode_paged",
     "decode_workspace_bytes", "status_string", "last_device_error", "load", "LIB_PATH", "DiffAttnError",
     "SUPPORTED_WIDTHS",
 ]
@@ -61,6 +61,9 @@ def load():
     lib.diffattn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, i32, i32, i32,
                                           vp, f32, i32, vp, sz, vp, vp, vp]
     lib.diffattn_decode_paged.restype = i32
+    lib.diffattn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32, vp, f32,
+                                     vp, vp, vp]
+    lib.diffattn_fwd_fp8.restype = i32
     lib.diffattn_fwd_train.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32, vp, f32,
                                        vp, vp, vp, vp, vp]
     lib.diffattn_fwd_train.restype = i32
@@ -130,6 +133,35 @@ def fwd(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps=1e-5, ou
                                 _ptr(o_prenorm), _stream(stream))
     if rc != OK:
         raise DiffAttnError(rc, "diffattn_fwd")
+    return out
+
+
+def fwd_fp8(q1, k1, q2, k2, v, qk_scale, lam, lam_init, causal=False, gamma=None, eps=1e-5, out=None,
+            o_prenorm=None, stream=None):
+    """Prefill forward with fp8 (e4m3) queries and keys.  q1, q2 [B,H,Nq,d] and
+    k1, k2 [B,H,Nk,d] are CUDA ``torch.float8_e4m3fn`` tensors; qk_scale is a
+    CUDA float32 tensor of 4*H per-head dequantisation scales (rows q1, k1,
+    q2, k2); v is bf16.  Returns out (bf16 [B,H,Nq,dv])."""
+    import torch
+    for n, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.float8_e4m3fn:
+            raise TypeError(f"{n} must be a CUDA float8_e4m3fn tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous 4-D tensor [B,H,N,d]")
+    _check_bf16("v", v)
+    B, H, Nq, d = q1.shape
+    Nk, dv = k1.shape[2], v.shape[3]
+    if (not qk_scale.is_cuda or qk_scale.dtype != torch.float32 or not qk_scale.is_contiguous()
+            or qk_scale.numel() != 4 * H):
+        raise ValueError("qk_scale must be a contiguous CUDA float32 tensor with 4*H entries")
+    if out is None:
+        out = torch.empty((B, H, Nq, dv), dtype=torch.bfloat16, device=q1.device)
+    g = _gamma(gamma, H, dv)
+    rc = load().diffattn_fwd_fp8(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), _ptr(qk_scale), float(lam),
+                                 float(lam_init), int(bool(causal)), B, H, Nq, Nk, d, dv, _ptr(g), float(eps),
+                                 _ptr(out), _ptr(o_prenorm), _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_fwd_fp8")
     return out
 
 

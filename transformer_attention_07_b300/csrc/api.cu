@@ -79,7 +79,27 @@ int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* 
     if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
     if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
     diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
-                            gn_gamma, out, o_prenorm, nullptr, nullptr};
+                            gn_gamma, out, o_prenorm, nullptr, nullptr, nullptr};
+    return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
+int diffattn_fwd_fp8(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                     const float* qk_scale, float lambda, float lambda_init, int causal, int B, int H, int Nq, int Nk,
+                     int d, int dv, const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !qk_scale || !out) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma) || !aligned4(qk_scale))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
+    diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
+                            gn_gamma, out, o_prenorm, nullptr, nullptr, qk_scale};
     return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -103,7 +123,7 @@ int diffattn_fwd_train(const void* q1, const void* k1, const void* q2, const voi
     if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
     if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
     diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
-                            gn_gamma, out, o_prenorm, o2, lse};
+                            gn_gamma, out, o_prenorm, o2, lse, nullptr};
     return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -66,16 +66,19 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D bf16 map over a BHND tensor [B][H][N][W]: dims (W, N, H, B).
+// 4-D map over a BHND tensor [B][H][N][W] of bf16 (or of bytes, esize 1):
+// dims (W, N, H, B).
 static bool make_map_bhnd(CUtensorMap* m, const void* base, int B, int H, int N, int W, int box_w, int box_n,
-                          CUtensorMapSwizzle swz) {
+                          CUtensorMapSwizzle swz, int esize = 2) {
     auto fn = encode_fn();
     if (!fn) return false;
+    const cuuint64_t e = (cuuint64_t)esize;
     const cuuint64_t dims[4] = {(cuuint64_t)W, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)W * 2, (cuuint64_t)N * W * 2, (cuuint64_t)H * N * W * 2};
+    const cuuint64_t strides[3] = {(cuuint64_t)W * e, (cuuint64_t)N * W * e, (cuuint64_t)H * N * W * e};
     const cuuint32_t box[4] = {(cuuint32_t)box_w, (cuuint32_t)box_n, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+    const CUtensorMapDataType dt = esize == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUresult r = fn(m, dt, 4, const_cast<void*>(base), dims, strides, box,
                           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS && std::getenv("DIFFATTN_DEBUG"))
@@ -85,15 +88,19 @@ static bool make_map_bhnd(CUtensorMap* m, const void* base, int B, int H, int N,
 
 // ----------------------------------------------------------------- prefill
 
-template <int D, int DV, bool CAUSAL>
+template <int D, int DV, bool CAUSAL, bool QK8>
 static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
-    using L = PrefillLayout<D, DV>;
+    using L = PrefillLayout<D, DV, QK8>;
     CUtensorMap mq1, mq2, mk1, mk2, mv;
-    const CUtensorMapSwizzle qk_swz = D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (!make_map_bhnd(&mq1, a.q1, a.B, a.H, a.Nq, D, D, L::BM, qk_swz) ||
-        !make_map_bhnd(&mq2, a.q2, a.B, a.H, a.Nq, D, D, L::BM, qk_swz) ||
-        !make_map_bhnd(&mk1, a.k1, a.B, a.H, a.Nk, D, D, L::BN, qk_swz) ||
-        !make_map_bhnd(&mk2, a.k2, a.B, a.H, a.Nk, D, D, L::BN, qk_swz) ||
+    // Q/K rows are one swizzle span wide (128, 64 or 32 bytes).
+    const CUtensorMapSwizzle qk_swz = L::QK_ROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                      : L::QK_ROW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_32B;
+    const int qe = (int)L::QK_ELEM;
+    if (!make_map_bhnd(&mq1, a.q1, a.B, a.H, a.Nq, D, D, L::BM, qk_swz, qe) ||
+        !make_map_bhnd(&mq2, a.q2, a.B, a.H, a.Nq, D, D, L::BM, qk_swz, qe) ||
+        !make_map_bhnd(&mk1, a.k1, a.B, a.H, a.Nk, D, D, L::BN, qk_swz, qe) ||
+        !make_map_bhnd(&mk2, a.k2, a.B, a.H, a.Nk, D, D, L::BN, qk_swz, qe) ||
         !make_map_bhnd(&mv, a.v, a.B, a.H, a.Nk, DV, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return LAUNCH_ERR_CUDA;
     PrefillParams p;
@@ -110,7 +117,8 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     p.o_prenorm = a.o_prenorm;
     p.o2 = a.o2;
     p.lse = a.lse;
-    auto kern = prefill_kernel<D, DV, CAUSAL>;
+    p.qk_scale = a.qk_scale;
+    auto kern = prefill_kernel<D, DV, CAUSAL, QK8>;
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
                  "prefill: set shared memory"))
         return LAUNCH_ERR_CUDA;
@@ -119,12 +127,17 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     return cuda_ok(cudaGetLastError(), "prefill: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }
 
-int launch_prefill(const PrefillArgs& a, cudaStream_t st) {
+template <bool QK8>
+static int launch_prefill_q(const PrefillArgs& a, cudaStream_t st) {
     if (a.d == 64 && a.dv == 128)
-        return a.causal ? launch_prefill_t<64, 128, true>(a, st) : launch_prefill_t<64, 128, false>(a, st);
+        return a.causal ? launch_prefill_t<64, 128, true, QK8>(a, st) : launch_prefill_t<64, 128, false, QK8>(a, st);
     if (a.d == 32 && a.dv == 64)
-        return a.causal ? launch_prefill_t<32, 64, true>(a, st) : launch_prefill_t<32, 64, false>(a, st);
+        return a.causal ? launch_prefill_t<32, 64, true, QK8>(a, st) : launch_prefill_t<32, 64, false, QK8>(a, st);
     return LAUNCH_ERR_UNSUPPORTED;
+}
+
+int launch_prefill(const PrefillArgs& a, cudaStream_t st) {
+    return a.qk_scale ? launch_prefill_q<true>(a, st) : launch_prefill_q<false>(a, st);
 }
 
 // ----------------------------------------------------------------- backward

@@ -23,6 +23,7 @@ struct PrefillArgs {
     float* o_prenorm;
     float* o2;    // training outputs (null for inference)
     float* lse;
+    const float* qk_scale;   // non-null: q1, k1, q2, k2 are e4m3 with these [4,H] per-head scales
 };
 
 struct DecodeArgs {

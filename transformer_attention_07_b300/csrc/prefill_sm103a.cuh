@@ -48,16 +48,22 @@ struct PrefillParams {
     float* o_prenorm;       // fp32 [B,H,Nq,dv] or null
     float* o2;              // fp32 [B,H,Nq,dv] or null: A2 V (the second map's normalised output)
     float* lse;             // fp32 [2,B,H,Nq] or null: log sum_j exp(s_r,ij), natural log, per map
+    const float* qk_scale;  // [4,H] dequantisation scales of q1, k1, q2, k2 per head (fp8 inputs), or null
 };
 
-template <int D, int DV>
+// QK8: Q1, Q2, K1, K2 are fp8 (e4m3) with per-head scales, and Q K^T runs
+// as an 8-bit tensor-core product (kind::f8f6f4, K = 32 per instruction);
+// P V stays bf16.
+template <int D, int DV, bool QK8 = false>
 struct PrefillLayout {
     static constexpr int BM = 128;   // query rows per tile (MMA M)
     static constexpr int BN = 128;   // keys per tile (MMA N of QK^T, K of PV)
     static constexpr int KST = 3;    // K1/K2 ring depth
     static constexpr int VST = 2;    // V ring depth
-    static constexpr uint32_t Q_BYTES = BM * D * 2;
-    static constexpr uint32_t K_BYTES = BN * D * 2;
+    static constexpr uint32_t QK_ELEM = QK8 ? 1 : 2;   // bytes per Q/K element
+    static constexpr uint32_t QK_ROW = D * QK_ELEM;    // bytes per Q/K row: 128, 64 or 32
+    static constexpr uint32_t Q_BYTES = BM * QK_ROW;
+    static constexpr uint32_t K_BYTES = BN * QK_ROW;
     static constexpr uint32_t V_BOX = BN * 128;   // one 64-column V box: BN rows x 128 bytes
     static constexpr uint32_t V_BYTES = BN * DV * 2;
     static constexpr uint32_t OFF_Q1 = 0;
@@ -81,8 +87,10 @@ struct PrefillLayout {
     // +1024 for aligning the dynamic base; at least 120 KB so that a single
     // CTA (which takes all 512 TMEM columns) is resident per SM.
     static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u) ? USED + 1024 : 120u * 1024u;
-    static constexpr uint32_t QK_SWZ = (D == 64) ? SWZ_128B : SWZ_64B;
-    static constexpr uint32_t QK_SBO = 8 * D * 2;    // bytes between 8-row groups
+    // The swizzle span equals the row width, so each row is one span.
+    static constexpr uint32_t QK_SWZ = QK_ROW == 128 ? SWZ_128B : QK_ROW == 64 ? SWZ_64B : SWZ_32B;
+    static constexpr uint32_t QK_SBO = 8 * QK_ROW;   // bytes between 8-row groups
+    static constexpr int QK_KSTEPS = QK_ROW / 32;    // 32 bytes of the row per MMA (16 bf16 or 32 fp8)
     static constexpr uint32_t TM_S1 = 0, TM_S2 = 128, TM_O1 = 256, TM_O2 = 256 + DV;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 384;
@@ -91,12 +99,12 @@ struct PrefillLayout {
     static_assert(USED + 1024 <= 227u * 1024u, "shared memory");
 };
 
-template <int D, int DV, bool CAUSAL>
+template <int D, int DV, bool CAUSAL, bool QK8 = false>
 __global__ void __launch_bounds__(384, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
                const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
                const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using L = PrefillLayout<D, DV>;
+    using L = PrefillLayout<D, DV, QK8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_addr(smem);
@@ -189,7 +197,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(L::BM, L::BN, false);
+            constexpr uint32_t idesc_qk = QK8 ? idesc_e4m3_f32(L::BM, L::BN) : idesc_bf16_f32(L::BM, L::BN, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(L::BM, DV, true);
             bool ok = mbar_wait(bar(L::B_Q), 0, ERR_SITE_PREFILL_MMA);
             tc_fence_after();
@@ -213,7 +221,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             // S = Q K^T over one key tile: 16-column steps of d (32 bytes).
             auto qk = [&](uint32_t t_s, uint64_t dq, uint64_t dks) {
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) mma_ss(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk, k > 0 ? 1u : 0u);
+                for (int k = 0; k < L::QK_KSTEPS; ++k) {
+                    if constexpr (QK8)
+                        mma_ss_f8(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk, k > 0 ? 1u : 0u);
+                    else
+                        mma_ss(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk, k > 0 ? 1u : 0u);
+                }
             };
             for (int j = 0; j <= n_kv && ok; ++j) {
                 const int ks = j % L::KST;
@@ -271,7 +284,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         const uint32_t o_col = r ? L::TM_O2 : L::TM_O1;
         const int qi = q0 + row;
         const int kmax = CAUSAL ? min(qi + diag, p.Nk - 1) : p.Nk - 1;   // last visible key
-        const float sl2 = p.scale_log2;
+        // log2(e)/sqrt(d), times the map's q and k dequantisation scales.
+        float sl2 = p.scale_log2;
+        if constexpr (QK8) sl2 *= p.qk_scale[(2 * r) * p.H + h] * p.qk_scale[(2 * r + 1) * p.H + h];
         float m = -INFINITY;   // running max of scaled logits (log2 domain)
         float l = 0.f;         // running sum of the bf16-rounded probabilities
         bool ok = true;
@@ -366,8 +381,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         // the scaled logits (natural log; m is in log2 units) and A2 V.
         if (p.lse != nullptr && qi < p.Nq)
             p.lse[((size_t)r * p.B * p.H + (size_t)b * p.H + h) * p.Nq + qi] = (m + log2f(l)) * 0.6931471805599453f;
-        float* o2row = (p.o2 != nullptr && qi < p.Nq) ? p.o2 + rowoff : nullptr;
-        const float inv2n = 1.0f / epi[L::BM + row];
+        if (p.o2 != nullptr) {   // uniform: every lane takes part in the warp-wide TMEM loads
+            const float inv2n = 1.0f / epi[L::BM + row];
+#pragma unroll
+            for (int c = 0; c < HALF / 32; ++c) {
+                uint32_t bb[32];
+                tmem_ld32(tmem + t_lane + L::TM_O2 + c0 + 32u * c, bb);
+                if (qi < p.Nq) {
+                    float4* dst = reinterpret_cast<float4*>(p.o2 + rowoff + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        dst[i] = make_float4(__uint_as_float(bb[4 * i]) * inv2n, __uint_as_float(bb[4 * i + 1]) * inv2n,
+                                             __uint_as_float(bb[4 * i + 2]) * inv2n,
+                                             __uint_as_float(bb[4 * i + 3]) * inv2n);
+                }
+            }
+        }
         float o[HALF];
 #pragma unroll
         for (int c = 0; c < HALF / 32; ++c) {
@@ -379,13 +408,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 // Both products rounded before the subtraction (no FMA
                 // contraction), so identical maps with lambda = 1 cancel to 0.
                 o[32 * c + i] = __fmul_rn(__uint_as_float(a[i]), inv1) - __fmul_rn(__uint_as_float(bb[i]), inv2);
-            if (o2row) {
-                float4* dst = reinterpret_cast<float4*>(o2row + 32 * c);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(__uint_as_float(bb[4 * i]) * inv2n, __uint_as_float(bb[4 * i + 1]) * inv2n,
-                                         __uint_as_float(bb[4 * i + 2]) * inv2n, __uint_as_float(bb[4 * i + 3]) * inv2n);
-            }
         }
         float sum = 0.f;
 #pragma unroll

@@ -100,6 +100,28 @@ int diffattn_fwd_fp8(const void* q1, const void* k1, const void* q2, const void*
                      const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream);
 
 /*
+ * Prefill with host-resident tensors: the same operation as diffattn_fwd, with
+ * q1, k1, q2, k2, v and out in HOST memory (BHND bf16; page-locked memory
+ * lets the copies overlap the computation, pageable memory works but
+ * serialises them).  gn_gamma, if given, is a device pointer as elsewhere.
+ * The B*H heads are processed in chunks of heads_per_chunk heads of one
+ * batch entry (0 = about eight chunks per call): each chunk's inputs are
+ * copied to a device slot on an internal stream, the prefill kernel runs on
+ * `stream`, and the chunk's output is copied back on a second internal
+ * stream, with three slots in flight.
+ *   workspace   device memory of >= diffattn_fwd_host_workspace_bytes(...)
+ *               bytes, 256-byte aligned (the slots)
+ * The call only enqueues work.  `out` is complete when `stream` has
+ * completed.  The result equals diffattn_fwd's bit for bit.
+ */
+size_t diffattn_fwd_host_workspace_bytes(int B, int H, int Nq, int Nk, int d, int dv, int heads_per_chunk);
+int diffattn_fwd_host(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                      float lambda, float lambda_init, int causal,
+                      int B, int H, int Nq, int Nk, int d, int dv,
+                      const float* gn_gamma, float eps, void* out, int heads_per_chunk,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Training forward: diffattn_fwd_ex plus what the backward pass reads.
  *   o_prenorm   [B,H,Nq,dv] fp32, required: (A1 - lambda A2) V
  *   o2          [B,H,Nq,dv] fp32, required, 16-byte aligned: A2 V

@@ -31,7 +31,8 @@ def declared_functions():
 
 def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
-        "diffattn_fwd", "diffattn_fwd_ex", "diffattn_fwd_fp8", "diffattn_fwd_train", "diffattn_bwd_workspace_bytes", "diffattn_bwd",
+        "diffattn_fwd", "diffattn_fwd_ex", "diffattn_fwd_host", "diffattn_fwd_host_workspace_bytes", "diffattn_fwd_fp8",
+        "diffattn_fwd_train", "diffattn_bwd_workspace_bytes", "diffattn_bwd",
         "diffattn_decode_workspace_bytes", "diffattn_decode",
         "diffattn_decode_noalloc", "diffattn_decode_paged", "diffattn_standard_fwd", "diffattn_status_string",
         "diffattn_last_device_error"])
@@ -76,6 +77,27 @@ def test_fwd_empty_problems_return_ok_without_launch(lib):
     assert fwd(lib, H=0) == OK
     assert fwd(lib, Nq=0) == OK
     assert fwd(lib, Nq=0, causal=1) == OK
+
+
+def test_fwd_host_validation(lib):
+    hb = lib.diffattn_fwd_host_workspace_bytes
+    # three slots of (q1, q2, k1, k2, v, out) for a chunk of heads, each tensor 256-byte aligned
+    slot = lambda c, Nq, Nk, d, dv: sum((x + 255) // 256 * 256 for x in
+                                        (c * Nq * d * 2, c * Nq * d * 2, c * Nk * d * 2, c * Nk * d * 2,
+                                         c * Nk * dv * 2, c * Nq * dv * 2))
+    assert hb(1, 16, 100, 100, 64, 128, 0) == 3 * slot(2, 100, 100, 64, 128)      # auto: 16 heads / 8 chunks
+    assert hb(2, 3, 64, 96, 32, 64, 5) == 3 * slot(3, 64, 96, 32, 64)             # capped at H
+    assert hb(1, 0, 64, 64, 64, 128, 0) == 0
+    fh = lambda q=FAKE, out=FAKE, ws=ctypes.c_void_p(0x10000), wsb=1 << 30, d=64, dv=128, chunk=0, B=1: \
+        lib.diffattn_fwd_host(q, q, q, q, q, 0.5, 0.8, 0, B, 2, 64, 64, d, dv, None, 1e-5, out, chunk, ws, wsb, None)
+    assert fh(q=None) == INVALID
+    assert fh(out=None) == INVALID
+    assert fh(chunk=-1) == INVALID
+    assert fh(d=64, dv=64) == UNSUPPORTED
+    assert fh(ws=None) == WORKSPACE
+    assert fh(wsb=1024) == WORKSPACE
+    assert fh(ws=ctypes.c_void_p(0x10010)) == INVALID
+    assert fh(B=0) == OK
 
 
 def test_fwd_fp8_validation(lib):

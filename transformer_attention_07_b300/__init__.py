@@ -18,7 +18,7 @@ import ctypes
 import os
 
 __all__ = [
-    "fwd", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes", "standard_fwd", "decode", "decode_paged",
+    "fwd", "fwd_host", "fwd_host_workspace_bytes", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes", "standard_fwd", "decode", "decode_paged",
     "decode_workspace_bytes", "status_string", "last_device_error", "load", "LIB_PATH", "DiffAttnError",
     "SUPPORTED_WIDTHS",
 ]
@@ -61,6 +61,11 @@ def load():
     lib.diffattn_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, f32, f32, i32, i32, i32, i32,
                                           vp, f32, i32, vp, sz, vp, vp, vp]
     lib.diffattn_decode_paged.restype = i32
+    lib.diffattn_fwd_host_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.diffattn_fwd_host_workspace_bytes.restype = sz
+    lib.diffattn_fwd_host.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32, vp, f32, vp,
+                                      i32, vp, sz, vp]
+    lib.diffattn_fwd_host.restype = i32
     lib.diffattn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32, vp, f32,
                                      vp, vp, vp]
     lib.diffattn_fwd_fp8.restype = i32
@@ -133,6 +138,42 @@ def fwd(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps=1e-5, ou
                                 _ptr(o_prenorm), _stream(stream))
     if rc != OK:
         raise DiffAttnError(rc, "diffattn_fwd")
+    return out
+
+
+def fwd_host_workspace_bytes(B, H, Nq, Nk, d, dv, heads_per_chunk=0) -> int:
+    return int(load().diffattn_fwd_host_workspace_bytes(B, H, Nq, Nk, d, dv, heads_per_chunk))
+
+
+def fwd_host(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps=1e-5, out=None, heads_per_chunk=0,
+             workspace=None, stream=None, device=None):
+    """Prefill with host-resident tensors: q1,q2 [B,H,Nq,d], k1,k2 [B,H,Nk,d],
+    v [B,H,Nk,dv] are CPU bf16 tensors (page-locked for overlapped copies);
+    returns ``out`` (CPU bf16 [B,H,Nq,dv]).  The library copies chunks of heads
+    in, runs the kernel and copies the results out on its own streams.  The
+    call is asynchronous: ``out`` is complete once ``stream`` (default: torch's
+    current stream) has completed.  ``gamma`` is a CUDA tensor, as elsewhere."""
+    import torch
+    for n, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2), ("v", v)):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16:
+            raise TypeError(f"{n} must be a CPU bf16 tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous 4-D tensor [B,H,N,width]")
+    B, H, Nq, d = q1.shape
+    Nk, dv = k1.shape[2], v.shape[3]
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    if out is None:
+        out = torch.empty((B, H, Nq, dv), dtype=torch.bfloat16).pin_memory()
+    if workspace is None:
+        workspace = torch.empty(max(fwd_host_workspace_bytes(B, H, Nq, Nk, d, dv, heads_per_chunk), 256),
+                                dtype=torch.uint8, device=dev)
+    g = _gamma(gamma, H, dv)
+    rc = load().diffattn_fwd_host(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), float(lam), float(lam_init),
+                                  int(bool(causal)), B, H, Nq, Nk, d, dv, _ptr(g), float(eps), _ptr(out),
+                                  int(heads_per_chunk), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_fwd_host")
     return out
 
 

@@ -248,6 +248,34 @@ int diffattn_decode_paged(const void* q1, const void* q2, const void* k1_pages, 
                           void* out, float* o_prenorm, void* stream);
 
 /*
+ * Split-KV decode over key ranges held by different GPUs (sequence sharding
+ * for caches longer than one GPU holds).  Each GPU computes the partial
+ * softmax states of its own range; the states of all ranges are gathered
+ * (e.g. an all-gather over the GPUs) and merged.  The merge is the
+ * associativity of the online softmax, the same algebra that combines the
+ * key ranges of one GPU in diffattn_decode.
+ *
+ * diffattn_decode_partials: q1, q2 [B,H,1,d]; k1, k2 [B,H,Nk,d]; v [B,H,Nk,dv]
+ *   (this GPU's Nk keys) bf16.  Writes to `partials` (fp32, 16-byte aligned,
+ *   >= diffattn_decode_partials_bytes(B, H, dv, num_splits) bytes) the states
+ *   [B*H][num_splits][2 maps][dv + 4]: m (running max of the scaled logits, in
+ *   log2 units: logit * log2(e)), l (sum of 2^(logit*log2(e) - m)), two unused
+ *   words, then the dv-wide unnormalised output.  A range with no keys has
+ *   m = -inf, l = 0.  num_splits (1..64) must be the same on every GPU.
+ * diffattn_decode_merge: `partials` holds num_parts such blocks back to back
+ *   ([num_parts][B*H][num_splits][2][dv + 4], the layout of an all-gather);
+ *   writes out [B,H,1,dv] bf16 (and o_prenorm, if given) exactly as
+ *   diffattn_decode.  num_parts * num_splits <= 4096.
+ */
+size_t diffattn_decode_partials_bytes(int B, int H, int dv, int num_splits);
+int diffattn_decode_partials(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                             int B, int H, int Nk, int d, int dv, int num_splits,
+                             float* partials, size_t partials_bytes, void* stream);
+int diffattn_decode_merge(const float* partials, int num_parts, int B, int H, int dv, int num_splits,
+                          float lambda, float lambda_init, const float* gn_gamma, float eps,
+                          void* out, float* o_prenorm, void* stream);
+
+/*
  * Split-KV decode that allocates nothing: the same computation and arguments
  * as diffattn_decode, minus the workspace.  (The Differential Transformer
  * pages have no counterpart to this entry point; it exists for callers.)

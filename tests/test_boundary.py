@@ -33,7 +33,8 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "diffattn_fwd", "diffattn_fwd_ex", "diffattn_fwd_host", "diffattn_fwd_host_workspace_bytes", "diffattn_fwd_fp8",
         "diffattn_fwd_train", "diffattn_bwd_workspace_bytes", "diffattn_bwd",
-        "diffattn_decode_workspace_bytes", "diffattn_decode",
+        "diffattn_decode_workspace_bytes", "diffattn_decode", "diffattn_decode_partials_bytes",
+        "diffattn_decode_partials", "diffattn_decode_merge",
         "diffattn_decode_noalloc", "diffattn_decode_paged", "diffattn_standard_fwd", "diffattn_status_string",
         "diffattn_last_device_error"])
 
@@ -182,6 +183,29 @@ def test_decode_paged_validation(lib):
     assert pg(ws=None) == WORKSPACE
     assert pg(max_pages=2048, page_size=32, splits=1) == INVALID   # one range would span > 1024 pages
     assert pg(B=0) == OK
+
+
+def test_decode_partials_and_merge_validation(lib):
+    assert lib.diffattn_decode_partials_bytes(2, 3, 128, 4) == 2 * 3 * 4 * 2 * (128 + 4) * 4
+    assert lib.diffattn_decode_partials_bytes(2, 3, 128, 0) == 0
+    dp = lambda q=FAKE, splits=2, d=64, dv=128, buf=FAKE, nb=1 << 20, B=1: lib.diffattn_decode_partials(
+        q, q, q, q, q, B, 2, 64, d, dv, splits, buf, nb, None)
+    assert dp(q=None) == INVALID
+    assert dp(splits=0) == INVALID
+    assert dp(splits=65) == INVALID
+    assert dp(d=32, dv=128) == UNSUPPORTED
+    assert dp(buf=None) == WORKSPACE
+    assert dp(nb=64) == WORKSPACE
+    assert dp(buf=ctypes.c_void_p(0x10004)) == INVALID
+    assert dp(B=0) == OK
+    dm = lambda parts=2, splits=2, dv=128, out=FAKE, B=1, lam=0.5: lib.diffattn_decode_merge(
+        FAKE, parts, B, 2, dv, splits, lam, 0.8, None, 1e-5, out, None, None)
+    assert dm(parts=0) == INVALID
+    assert dm(parts=100, splits=64) == INVALID     # more than 4096 partial states per head
+    assert dm(out=None) == INVALID
+    assert dm(dv=96) == UNSUPPORTED
+    assert dm(lam=float("nan")) == INVALID
+    assert dm(B=0) == OK
 
 
 def test_decode_workspace_bytes(lib):

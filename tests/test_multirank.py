@@ -54,3 +54,40 @@ def test_single_rank_is_identity():
     sys.path.insert(0, ROOT)
     import bench
     assert bench.reduce_max_over_ranks([1.0, 2.0], 1, None) == [1.0, 2.0]
+
+
+def _gather_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import transformer_attention_07_b300 as da
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        # a rank's partial states: [B*H, splits, 2, dv + 4], tagged with the rank
+        part = torch.full((3, 2, 2, 8), float(rank)) + torch.arange(3 * 2 * 2 * 8, dtype=torch.float32).view(3, 2, 2, 8)
+        got = da.gather_partials(part)
+        q.put((rank, got.shape, got[:, 0, 0, 0, 0].tolist(), torch.equal(got[rank], part)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gather_partials_stacks_ranks_in_order():
+    """The exchange step of sequence-sharded decode: every rank receives all
+    ranks' partial states, stacked in rank order (the [parts, ...] layout the
+    merge kernel reads)."""
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_gather_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, shape, firsts, own in results:
+        assert tuple(shape) == (2, 3, 2, 2, 8)
+        assert firsts == [0.0, 1.0]
+        assert own

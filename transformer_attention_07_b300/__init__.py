@@ -19,7 +19,8 @@ import os
 
 __all__ = [
     "fwd", "fwd_host", "fwd_host_workspace_bytes", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes", "standard_fwd", "decode", "decode_paged",
-    "decode_workspace_bytes", "status_string", "last_device_error", "load", "LIB_PATH", "DiffAttnError",
+    "decode_workspace_bytes", "decode_partials", "decode_partials_bytes", "decode_merge", "gather_partials",
+    "decode_sharded", "status_string", "last_device_error", "load", "LIB_PATH", "DiffAttnError",
     "SUPPORTED_WIDTHS",
 ]
 
@@ -77,6 +78,12 @@ def load():
     lib.diffattn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, i32, i32,
                                  vp, f32, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     lib.diffattn_bwd.restype = i32
+    lib.diffattn_decode_partials_bytes.argtypes = [i32, i32, i32, i32]
+    lib.diffattn_decode_partials_bytes.restype = sz
+    lib.diffattn_decode_partials.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, sz, vp]
+    lib.diffattn_decode_partials.restype = i32
+    lib.diffattn_decode_merge.argtypes = [vp, i32, i32, i32, i32, i32, f32, f32, vp, f32, vp, vp, vp]
+    lib.diffattn_decode_merge.restype = i32
     lib.diffattn_standard_fwd.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]
     lib.diffattn_standard_fwd.restype = i32
     lib.diffattn_status_string.argtypes = [i32]
@@ -344,6 +351,71 @@ def decode_paged(q1, q2, k1_pages, k2_pages, v_pages, block_table, seq_lens, lam
     if rc != OK:
         raise DiffAttnError(rc, "diffattn_decode_paged")
     return out
+
+
+def decode_partials_bytes(B, H, dv, num_splits) -> int:
+    return int(load().diffattn_decode_partials_bytes(B, H, dv, num_splits))
+
+
+def decode_partials(q1, k1, q2, k2, v, num_splits, partials=None, stream=None):
+    """Partial softmax states of this GPU's key range (see include/diffattn.h):
+    returns an fp32 CUDA tensor [B*H, num_splits, 2, dv + 4]."""
+    import torch
+    for n, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2), ("v", v)):
+        _check_bf16(n, t)
+    B, H, _, d = q1.shape
+    Nk, dv = k1.shape[2], v.shape[3]
+    if partials is None:
+        partials = torch.empty((B * H, num_splits, 2, dv + 4), dtype=torch.float32, device=q1.device)
+    rc = load().diffattn_decode_partials(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), B, H, Nk, d, dv,
+                                         int(num_splits), _ptr(partials),
+                                         partials.numel() * partials.element_size(), _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_decode_partials")
+    return partials
+
+
+def decode_merge(partials, B, H, lam, lam_init, gamma=None, eps=1e-5, out=None, o_prenorm=None, stream=None):
+    """Merge gathered partial states [num_parts, B*H, num_splits, 2, dv + 4]
+    (or one part without the leading dimension); returns out [B,H,1,dv] bf16."""
+    import torch
+    if partials.dim() == 4:
+        partials = partials.unsqueeze(0)
+    if not partials.is_cuda or partials.dtype != torch.float32 or not partials.is_contiguous():
+        raise TypeError("partials must be a contiguous CUDA float32 tensor")
+    parts, bh, splits, two, w = partials.shape
+    dv = w - 4
+    if bh != B * H or two != 2:
+        raise ValueError("partials must be [num_parts, B*H, num_splits, 2, dv + 4]")
+    if out is None:
+        out = torch.empty((B, H, 1, dv), dtype=torch.bfloat16, device=partials.device)
+    g = _gamma(gamma, H, dv)
+    rc = load().diffattn_decode_merge(_ptr(partials), parts, B, H, dv, splits, float(lam), float(lam_init), _ptr(g),
+                                      float(eps), _ptr(out), _ptr(o_prenorm), _stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_decode_merge")
+    return out
+
+
+def gather_partials(partials, group=None):
+    """All-gather the partial states of every rank of ``group`` (torch.distributed):
+    returns [world, *partials.shape], rank order, the layout decode_merge reads.
+    This is the one exchange step of sequence-sharded decode."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    chunks = [torch.empty_like(partials) for _ in range(world)]
+    dist.all_gather(chunks, partials.contiguous(), group=group)
+    return torch.stack(chunks)
+
+
+def decode_sharded(q1, k1, q2, k2, v, lam, lam_init, num_splits=8, gamma=None, eps=1e-5, group=None, stream=None):
+    """Split-KV decode with the key cache sharded over the ranks of ``group``:
+    every rank passes the same queries and its own slice of K1, K2, V; the
+    ranks' partial states are all-gathered and merged on every rank."""
+    B, H = q1.shape[:2]
+    part = decode_partials(q1, k1, q2, k2, v, num_splits, stream=stream)
+    return decode_merge(gather_partials(part, group), B, H, lam, lam_init, gamma=gamma, eps=eps, stream=stream)
 
 
 def last_device_error(stream=None) -> int:

@@ -232,8 +232,53 @@ int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* 
     const int per = (Nk + splits - 1) / splits;
     const int keys_per_split = (per + 31) / 32 * 32;
     diffattn::DecodeArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, B, H, Nk, d, dv,
-                           splits, keys_per_split, gn_gamma, static_cast<float*>(workspace), out, o_prenorm};
+                           splits, keys_per_split, gn_gamma, static_cast<float*>(workspace), out, o_prenorm,
+                           nullptr, nullptr, 0, 0, 0, false};
     return from_launch(diffattn::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+size_t diffattn_decode_partials_bytes(int B, int H, int dv, int num_splits) {
+    if (B < 0 || H < 0 || dv < 1 || num_splits < 1 || num_splits > kMaxSplits) return 0;
+    return workspace_for(B, H, dv, num_splits);
+}
+
+int diffattn_decode_partials(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, int B,
+                             int H, int Nk, int d, int dv, int num_splits, float* partials, size_t partials_bytes,
+                             void* stream) {
+    if (!q1 || !k1 || !q2 || !k2 || !v) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (num_splits < 1 || num_splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H * Nk >= (int64_t(1) << 31) - 64) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H == 0) return DIFFATTN_OK;
+    if (!partials || partials_bytes < workspace_for(B, H, dv, num_splits)) return DIFFATTN_ERR_WORKSPACE;
+    if (!aligned16(partials)) return DIFFATTN_ERR_INVALID_ARG;
+    const int per = (Nk + num_splits - 1) / num_splits;
+    const int keys_per_split = (per + 31) / 32 * 32;
+    // lambda, lambda_init, eps, gamma and out belong to the merge; the split
+    // kernel does not read them.
+    diffattn::DecodeArgs a{q1, k1, q2, k2, v, 0.0f, 0.0f, 0.0f, B, H, Nk, d, dv, num_splits, keys_per_split,
+                           nullptr, partials, nullptr, nullptr, nullptr, nullptr, 0, 0, 0, true};
+    return from_launch(diffattn::launch_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
+int diffattn_decode_merge(const float* partials, int num_parts, int B, int H, int dv, int num_splits, float lambda,
+                          float lambda_init, const float* gn_gamma, float eps, void* out, float* o_prenorm,
+                          void* stream) {
+    if (!partials || !out) return DIFFATTN_ERR_INVALID_ARG;
+    if (num_parts < 1 || B < 0 || H < 0 || num_splits < 1 || num_splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)num_parts * num_splits > 4096) return DIFFATTN_ERR_INVALID_ARG;
+    if (dv != 128 && dv != 64) return DIFFATTN_ERR_UNSUPPORTED;
+    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
+    if (!aligned16(partials) || !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)B * H == 0) return DIFFATTN_OK;
+    diffattn::MergeArgs a{partials, num_parts, B, H, num_splits, dv, lambda, lambda_init, eps, gn_gamma, out,
+                          o_prenorm};
+    return from_launch(diffattn::launch_decode_merge(a, static_cast<cudaStream_t>(stream)));
 }
 
 // Decode for callers that cannot allocate device memory: the split partials
@@ -297,7 +342,7 @@ int diffattn_decode_paged(const void* q1, const void* q2, const void* k1_pages, 
     const int keys_per_split = (per + 31) / 32 * 32;
     diffattn::DecodeArgs a{q1, k1_pages, q2, k2_pages, v_pages, lambda, lambda_init, eps, B, H, max_len, d, dv,
                            splits, keys_per_split, gn_gamma, static_cast<float*>(workspace), out, o_prenorm,
-                           block_table, seq_lens, max_pages, page_size, num_pages};
+                           block_table, seq_lens, max_pages, page_size, num_pages, false};
     return from_launch(diffattn::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 

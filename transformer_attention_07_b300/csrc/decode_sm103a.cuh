@@ -48,6 +48,7 @@ struct DecodeParams {
 
 struct MergeParams {
     int B, H, S;
+    int parts;            // partial sets gathered from separate key ranges (1 on one GPU)
     float lambda, lambda_init, eps;
     const float* ws;
     const float* gamma;   // [H*DV] or null
@@ -318,23 +319,29 @@ decode_merge_kernel(const MergeParams p) {
     const size_t bh = (size_t)blockIdx.x * 4 + warp;
     if (bh >= (size_t)p.B * p.H) return;
     const int h = (int)(bh % p.H);
-    const float* part = p.ws + bh * p.S * 2 * PART;
+    // Partial t = (part, split) of this head: parts are [parts][B*H][S] blocks.
+    const size_t BH = (size_t)p.B * p.H;
+    const int T = p.parts * p.S;
+    auto part = [&](int t, int r) -> const float* {
+        const int pt = t / p.S, s = t - pt * p.S;
+        return p.ws + ((((size_t)pt * BH + bh) * p.S + s) * 2 + r) * PART;
+    };
     float O[2][CPL], Lr[2];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         float M = -INFINITY;
-        for (int s = lane; s < p.S; s += 32) M = fmaxf(M, part[(s * 2 + r) * PART]);
+        for (int t = lane; t < T; t += 32) M = fmaxf(M, part(t, r)[0]);
         M = warp_max(M);
         float Ls = 0.f;
-        for (int s = lane; s < p.S; s += 32) {
-            const float m = part[(s * 2 + r) * PART];
-            if (m != -INFINITY) Ls = fmaf(part[(s * 2 + r) * PART + 1], fast_exp2(m - M), Ls);
+        for (int t = lane; t < T; t += 32) {
+            const float m = part(t, r)[0];
+            if (m != -INFINITY) Ls = fmaf(part(t, r)[1], fast_exp2(m - M), Ls);
         }
         Lr[r] = warp_sum(Ls);
 #pragma unroll
         for (int i = 0; i < CPL; ++i) O[r][i] = 0.f;
-        for (int s = 0; s < p.S; ++s) {
-            const float* src = part + (s * 2 + r) * PART;
+        for (int t = 0; t < T; ++t) {
+            const float* src = part(t, r);
             const float m = src[0];
             if (m == -INFINITY) continue;
             const float e = fast_exp2(m - M);

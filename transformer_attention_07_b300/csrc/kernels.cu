@@ -308,10 +308,12 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
         return LAUNCH_ERR_CUDA;
     kern<<<dim3(a.splits, a.H, a.B), L::THREADS, L::SMEM_BYTES, st>>>(mk1, mk2, p);
     if (!cuda_ok(cudaGetLastError(), "decode: split launch")) return LAUNCH_ERR_CUDA;
+    if (a.partials_only) return LAUNCH_OK;
     MergeParams mp;
     mp.B = a.B;
     mp.H = a.H;
     mp.S = a.splits;
+    mp.parts = 1;
     mp.lambda = a.lambda;
     mp.lambda_init = a.lambda_init;
     mp.eps = a.eps;
@@ -322,6 +324,29 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     const int heads = a.B * a.H;
     decode_merge_kernel<DV><<<(heads + 3) / 4, 128, 0, st>>>(mp);
     return cuda_ok(cudaGetLastError(), "decode: merge launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+}
+
+int launch_decode_merge(const MergeArgs& a, cudaStream_t st) {
+    MergeParams mp;
+    mp.B = a.B;
+    mp.H = a.H;
+    mp.S = a.splits;
+    mp.parts = a.parts;
+    mp.lambda = a.lambda;
+    mp.lambda_init = a.lambda_init;
+    mp.eps = a.eps;
+    mp.ws = a.ws;
+    mp.gamma = a.gamma;
+    mp.out = static_cast<uint16_t*>(a.out);
+    mp.o_prenorm = a.o_prenorm;
+    const int heads = a.B * a.H;
+    if (a.dv == 128)
+        decode_merge_kernel<128><<<(heads + 3) / 4, 128, 0, st>>>(mp);
+    else if (a.dv == 64)
+        decode_merge_kernel<64><<<(heads + 3) / 4, 128, 0, st>>>(mp);
+    else
+        return LAUNCH_ERR_UNSUPPORTED;
+    return cuda_ok(cudaGetLastError(), "decode: merge of gathered partials") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t st) {

@@ -39,7 +39,19 @@ struct DecodeArgs {
     const int32_t* block_table;
     const int32_t* seq_lens;
     int max_pages, page_size, num_pages;
+    bool partials_only;   // stop after the split kernel (the partials stay in ws)
 };
+
+// Merge of gathered decode partials: ws holds [parts][B*H][splits][2][dv + 4].
+struct MergeArgs {
+    const float* ws;
+    int parts, B, H, splits, dv;
+    float lambda, lambda_init, eps;
+    const float* gamma;
+    void* out;
+    float* o_prenorm;
+};
+int launch_decode_merge(const MergeArgs& a, cudaStream_t st);
 
 // With DIFFATTN_DEBUG set in the environment, a failing CUDA call is
 // reported on stderr (call site and the runtime's error string).

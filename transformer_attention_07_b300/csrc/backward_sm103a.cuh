@@ -23,9 +23,10 @@
 //   bwd_prep_kernel     one warp per row: GroupNorm backward, do (bf16),
 //                       D1, D2, per-row constants for the tile kernels, and
 //                       fixed-order partial sums of dgamma and dlambda.
-//   bwd_dq_kernel       one CTA per 128 query rows; walks the key tiles:
+//   bwd_dq_kernel       one CTA per 128 query rows; walks 128-key tiles:
 //                       S_r = Q_r K_r^T, dP = dO V^T on the tensor core,
-//                       dS_r in registers, dQ_r += dS_r K_r (dS_r from TMEM).
+//                       dS_r in registers, dQ_r += dS_r K_r (dS_r from TMEM);
+//                       the next tile's scores follow each map's dQ product.
 //   bwd_dkv_kernel      one CTA per 128 keys; walks the query tiles:
 //                       S_r^T = K_r Q_r^T, dP^T = V dO^T, then
 //                       dV += (A1 - lambda A2)^T dO, dK_r += dS_r^T Q_r.
@@ -213,11 +214,29 @@ __global__ void __launch_bounds__(256) bwd_finalize_kernel(const BwdParams p) {
 
 // ----------------------------------------------------------------- dQ sweep
 
+// Two 32-column TMEM loads of this thread's lane, then one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&a)[32], uint32_t tb, uint32_t (&b)[32]) {
+#define DA_R8(x, i) "=r"(x[i]), "=r"(x[i + 1]), "=r"(x[i + 2]), "=r"(x[i + 3]), "=r"(x[i + 4]), "=r"(x[i + 5]), \
+                    "=r"(x[i + 6]), "=r"(x[i + 7])
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47,"
+        " %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : DA_R8(a, 0), DA_R8(a, 8), DA_R8(a, 16), DA_R8(a, 24), DA_R8(b, 0), DA_R8(b, 8), DA_R8(b, 16), DA_R8(b, 24)
+        : "r"(ta), "r"(tb)
+        : "memory");
+#undef DA_R8
+}
+
 template <int D, int DV>
 struct BwdDqLayout {
     static constexpr int BM = 128;   // query rows per CTA (MMA M)
-    static constexpr int BN = 64;    // keys per tile
-    static constexpr int KST = 3;    // K1/K2/V ring depth
+    static constexpr int BN = 128;   // keys per tile (MMA N of S and dP)
+    static constexpr int KST = 2;    // K1/K2/V ring depth
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t DO_BOX = BM * 128;       // one 64-column box of dO
     static constexpr uint32_t DO_BYTES = BM * DV * 2;
@@ -233,18 +252,17 @@ struct BwdDqLayout {
     static constexpr int B_Q = 0;
     static constexpr int B_KFULL = 1;
     static constexpr int B_KEMPTY = B_KFULL + KST;
-    static constexpr int B_SFULL = B_KEMPTY + KST;   // [map][buffer]
-    static constexpr int B_PFULL = B_SFULL + 4;      // [map][buffer]
-    static constexpr int B_DQFULL = B_PFULL + 4;
+    static constexpr int B_SFULL = B_KEMPTY + KST;   // [map]: S_r (and dP) of the tile in TMEM
+    static constexpr int B_DPFREE = B_SFULL + 2;     // both maps have dP in registers
+    static constexpr int B_PFULL = B_DPFREE + 1;     // [map]: dS_r written over S_r
+    static constexpr int B_DQFULL = B_PFULL + 2;
     static constexpr int NBAR = B_DQFULL + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
     static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
     static constexpr uint32_t SMEM_BYTES = USED + 1024;
-    // Tensor memory: two buffers of (S1, S2, dP), 64 columns each, then the
-    // two dQ accumulators.  dS_r (bf16) is written over the first 32 columns
-    // of S_r.
-    static constexpr uint32_t TM_BUF = 192, TM_S1 = 0, TM_S2 = 64, TM_DP = 128;
-    static constexpr uint32_t TM_DQ1 = 384, TM_DQ2 = 448;
+    // Tensor memory: S1, S2, dP (128 columns each; dS_r in bf16 is written
+    // over the first 64 columns of S_r), then the two dQ accumulators.
+    static constexpr uint32_t TM_S1 = 0, TM_S2 = 128, TM_DP = 256, TM_DQ1 = 384, TM_DQ2 = 448;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 320;
     static_assert(D == 64 && DV == 128, "backward widths");
@@ -281,10 +299,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             mbar_init(bar(L::B_KFULL + s), 1);
             mbar_init(bar(L::B_KEMPTY + s), 1);
         }
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(bar(L::B_SFULL + i), 1);
-            mbar_init(bar(L::B_PFULL + i), 4);
+        for (int r = 0; r < 2; ++r) {
+            mbar_init(bar(L::B_SFULL + r), 1);
+            mbar_init(bar(L::B_PFULL + r), 4);
         }
+        mbar_init(bar(L::B_DPFREE), 8);
         mbar_init(bar(L::B_DQFULL), 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_q1);
@@ -349,51 +368,62 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             const uint64_t dkm0 = smem_desc(sb + L::OFF_K, L::K_BYTES, 1024, SWZ_128B);          // K1 as MN-major B
             const uint64_t dv0 = smem_desc(sb + L::OFF_K + 2 * L::K_BYTES, 16, 1024, SWZ_128B);  // V, stage 0
             constexpr uint64_t STAGE16 = L::STAGE >> 4, K2OFF = L::K_BYTES >> 4;
-            for (int j = 0; j <= n_kv && ok; ++j) {
-                if (j < n_kv) {
-                    const int ks = j % L::KST;
-                    ok = mbar_wait(bar(L::B_KFULL + ks), (j / L::KST) & 1, ERR_SITE_BWD_MMA);
+            // dP = dO V^T: k over dv, two 64-column boxes of each operand.
+            auto dp_mma = [&](uint64_t so) {
+#pragma unroll
+                for (int k = 0; k < DV / 16; ++k)
+                    mma_ss(tmem + L::TM_DP, ddo + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4),
+                           dv0 + so + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4), idesc_s,
+                           k > 0 ? 1u : 0u);
+            };
+            // S_r = Q_r K_r^T.
+            auto s_mma = [&](int r, uint64_t so) {
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                    mma_ss(tmem + (r ? L::TM_S2 : L::TM_S1), (r ? dq2 : dq1) + (uint64_t)(2 * k),
+                           dk0 + so + (r ? K2OFF : 0) + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
+            };
+            // dQ_r += dS_r K_r: dS_r (bf16) in the first 64 columns of S_r,
+            // 8 columns per 16 keys; the K tile read MN-major.
+            auto dq_mma = [&](int r, uint64_t so, bool first) {
+#pragma unroll
+                for (int k = 0; k < L::BN / 16; ++k)
+                    mma_ts(tmem + (r ? L::TM_DQ2 : L::TM_DQ1), tmem + (r ? L::TM_S2 : L::TM_S1) + 8u * k,
+                           dkm0 + so + (r ? K2OFF : 0) + (uint64_t)(k * (16 * 128 >> 4)), idesc_dq,
+                           (!first || k > 0) ? 1u : 0u);
+            };
+            if (ok) ok = mbar_wait(bar(L::B_KFULL + 0), 0, ERR_SITE_BWD_MMA);
+            if (ok) {
+                tc_fence_after();
+                dp_mma(0);
+                s_mma(0, 0);
+                mma_commit(bar(L::B_SFULL + 0));
+                s_mma(1, 0);
+                mma_commit(bar(L::B_SFULL + 1));
+            }
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const uint64_t so = (uint64_t)(j % L::KST) * STAGE16;
+                const bool more = j + 1 < n_kv;
+                const uint64_t sn = (uint64_t)((j + 1) % L::KST) * STAGE16;
+                if (more) {
+                    // dP of the next tile once both maps hold this tile's dP.
+                    ok = mbar_wait(bar(L::B_KFULL + (j + 1) % L::KST), ((j + 1) / L::KST) & 1, ERR_SITE_BWD_MMA);
+                    ok = ok && mbar_wait(bar(L::B_DPFREE), j & 1, ERR_SITE_BWD_MMA);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t tb = tmem + (uint32_t)(j & 1) * L::TM_BUF;
-                    const uint64_t so = (uint64_t)ks * STAGE16;
-                    // dP = dO V^T: k over dv, two 64-column boxes of each operand.
-#pragma unroll
-                    for (int k = 0; k < DV / 16; ++k)
-                        mma_ss(tb + L::TM_DP, ddo + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4),
-                               dv0 + so + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4), idesc_s,
-                               k > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k)
-                        mma_ss(tb + L::TM_S1, dq1 + (uint64_t)(2 * k), dk0 + so + (uint64_t)(2 * k), idesc_s,
-                               k > 0 ? 1u : 0u);
-                    mma_commit(bar(L::B_SFULL + 0 * 2 + (j & 1)));
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k)
-                        mma_ss(tb + L::TM_S2, dq2 + (uint64_t)(2 * k), dk0 + so + K2OFF + (uint64_t)(2 * k), idesc_s,
-                               k > 0 ? 1u : 0u);
-                    mma_commit(bar(L::B_SFULL + 1 * 2 + (j & 1)));
+                    dp_mma(sn);
                 }
-                if (j >= 1) {
-                    // dQ_r += dS_r K_r for the previous tile; dS_r (bf16) sits
-                    // in the first 32 columns of S_r, 8 columns per 16 keys.
-                    const int jp = j - 1;
-                    const int ksp = jp % L::KST;
-                    const uint32_t tb = tmem + (uint32_t)(jp & 1) * L::TM_BUF;
-                    const uint64_t so = (uint64_t)ksp * STAGE16;
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        ok = mbar_wait(bar(L::B_PFULL + r * 2 + (jp & 1)), (jp >> 1) & 1, ERR_SITE_BWD_MMA);
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int k = 0; k < L::BN / 16; ++k)
-                            mma_ts(tmem + (r ? L::TM_DQ2 : L::TM_DQ1), tb + (r ? L::TM_S2 : L::TM_S1) + 8u * k,
-                                   dkm0 + so + (r ? K2OFF : 0) + (uint64_t)(k * (16 * 128 >> 4)), idesc_dq,
-                                   (jp > 0 || k > 0) ? 1u : 0u);
-                    }
+                for (int r = 0; r < 2; ++r) {
+                    ok = mbar_wait(bar(L::B_PFULL + r), j & 1, ERR_SITE_BWD_MMA);
                     if (!ok) break;
-                    mma_commit(bar(L::B_KEMPTY + ksp));
+                    tc_fence_after();
+                    dq_mma(r, so, j == 0);
+                    if (r == 1) mma_commit(bar(L::B_KEMPTY + j % L::KST));
+                    if (more) {
+                        s_mma(r, sn);
+                        mma_commit(bar(L::B_SFULL + r));
+                    }
                 }
             }
             mma_commit(bar(L::B_DQFULL));
@@ -412,36 +442,48 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         const float Dr = r ? rc.w : rc.z;
         const float coef = r ? -p.lambda : 1.0f;
         const float sl2 = p.scale_log2;
-        const uint32_t s_col = r ? L::TM_S2 : L::TM_S1;
+        const uint32_t s_col = tmem + t_lane + (r ? L::TM_S2 : L::TM_S1);
+        const uint32_t dp_col = tmem + t_lane + L::TM_DP;
         bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            ok = mbar_wait(bar(L::B_SFULL + r * 2 + (j & 1)), (j >> 1) & 1, ERR_SITE_BWD_SOFTMAX);
+            ok = mbar_wait(bar(L::B_SFULL + r), j & 1, ERR_SITE_BWD_SOFTMAX);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t tb = tmem + t_lane + (uint32_t)(j & 1) * L::TM_BUF;
-            uint32_t sv[64], dp[64];
-            tmem_ld64(tb + s_col, sv);
-            tmem_ld64(tb + L::TM_DP, dp);
             const int kb = j * L::BN;
-            if (kb + L::BN - 1 > kmax) {
+            const bool edge = kb + L::BN - 1 > kmax;
+            // Four 32-key chunks; chunk c's bf16 dS lands in columns [16c, 16c+16),
+            // which this thread has already read.
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    if (kb + i > kmax) sv[i] = __float_as_uint(-INFINITY);
-            }
-            uint32_t pk[32];
+            for (int c = 0; c < 4; ++c) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32x2(s_col + 32u * c, sv, dp_col + 32u * c, dp);
+                if (c == 3) {
+                    // dP is in registers for this map: the next tile's dP may
+                    // overwrite it once the other map is there too.
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(L::B_DPFREE));
+                }
+                if (edge) {
 #pragma unroll
-            for (int i = 0; i < 64; i += 2) {
-                float x0, x1;
-                fma2_bcast(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), sl2, nlse);
-                const float p0 = fast_exp2(x0) * coef, p1 = fast_exp2(x1) * coef;
-                pk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - Dr), p1 * (__uint_as_float(dp[i + 1]) - Dr));
+                    for (int i = 0; i < 32; ++i)
+                        if (kb + 32 * c + i > kmax) sv[i] = __float_as_uint(-INFINITY);
+                }
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float x0, x1;
+                    fma2_bcast(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), sl2, nlse);
+                    const float p0 = fast_exp2(x0) * coef, p1 = fast_exp2(x1) * coef;
+                    pk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - Dr), p1 * (__uint_as_float(dp[i + 1]) - Dr));
+                }
+                tmem_st16(s_col + 16u * c, pk);
             }
-            tmem_st32(tb + s_col, pk);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::B_PFULL + r * 2 + (j & 1)));
+            if (lane == 0) mbar_arrive(bar(L::B_PFULL + r));
         }
         // ------------------------------------------------------------ epilogue
         mbar_wait(bar(L::B_DQFULL), 0, ERR_SITE_BWD_EPILOGUE);

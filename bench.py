@@ -275,6 +275,49 @@ def paged_decode_throughput(dev, reps=10):
     return res
 
 
+def small_decode_latency(dev, reps=200):
+    """Latency of one small decode call (B1 H32, 4096 keys, d64 dv128: two
+    kernels of a few microseconds each), launched eagerly through the C ABI
+    and replayed from a CUDA graph that captured the same calls."""
+    import torch
+    import transformer_attention_07_b300 as da
+    g = torch.Generator(device=dev)
+    g.manual_seed(4100)
+    mk = lambda *s: torch.randn(s, generator=g, device=dev).to(torch.bfloat16)
+    B, H, N = 1, 32, 4096
+    q1, k1, q2, k2, v = mk(B, H, 1, 64), mk(B, H, N, 64), mk(B, H, 1, 64), mk(B, H, N, 64), mk(B, H, N, 128)
+    ws = torch.empty(da.decode_workspace_bytes(B, H, N, 128, 0), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, H, 1, 128), dtype=torch.bfloat16, device=dev)
+    side = torch.cuda.Stream(dev)
+    run = lambda st: da.decode(q1, k1, q2, k2, v, 0.6, 0.8, workspace=ws, out=out, stream=st)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for _ in range(10):
+            run(side)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(10):
+            run(torch.cuda.current_stream(dev))
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name, fn, calls in (("eager", lambda: run(stream), 1), ("graph", graph.replay, 10)):
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps // calls):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[f"{name}_us_per_call"] = e0.elapsed_time(e1) * 1e3 / (reps // calls * calls)
+    nbytes = B * H * (N * (2 * 64 + 128) + 2 * 64 + 128) * 2
+    res["graph_GB/s"] = nbytes / (res["graph_us_per_call"] * 1e-6) / 1e9
+    res["shape"] = f"B{B} H{H} Nk{N} d64 dv128, 10 calls per graph"
+    return res
+
+
 def fp8_throughput(dev, w, inp, reps=10):
     """The prefill with fp8 (e4m3) Q/K (per-head scales amax/448) against the
     bf16 prefill on the same workload.  TFLOP/s counts the same algorithmic
@@ -502,6 +545,7 @@ def run_cuda(args, world, rank, local):
         line["backward"] = backward_throughput(dev, wp, pin)
         line["fp8_qk"] = fp8_throughput(dev, wp, pin)
         line["fp8_qk"]["vs_bf16"] = line["prefill_ms"] / line["fp8_qk"]["ms"] - 1.0
+        line["decode_small_latency"] = small_decode_latency(dev)
     if do_pre and not args.no_cpu_baseline:
         cpu = [pin[k].cpu() for k in names]
         rows = sample_rows_uniform(wp.Nq, args.cpu_rows, 4242)

@@ -105,7 +105,7 @@ int diffattn_fwd_fp8(const void* q1, const void* k1, const void* q2, const void*
  * lets the copies overlap the computation, pageable memory works but
  * serialises them).  gn_gamma, if given, is a device pointer as elsewhere.
  * The B*H heads are processed in chunks of heads_per_chunk heads of one
- * batch entry (0 = about eight chunks per call): each chunk's inputs are
+ * batch entry (0 = about sixteen chunks per call): each chunk's inputs are
  * copied to a device slot on an internal stream, the prefill kernel runs on
  * `stream`, and the chunk's output is copied back on a second internal
  * stream, with three slots in flight.

@@ -86,7 +86,8 @@ def test_fwd_host_validation(lib):
     slot = lambda c, Nq, Nk, d, dv: sum((x + 255) // 256 * 256 for x in
                                         (c * Nq * d * 2, c * Nq * d * 2, c * Nk * d * 2, c * Nk * d * 2,
                                          c * Nk * dv * 2, c * Nq * dv * 2))
-    assert hb(1, 16, 100, 100, 64, 128, 0) == 3 * slot(2, 100, 100, 64, 128)      # auto: 16 heads / 8 chunks
+    assert hb(1, 16, 100, 100, 64, 128, 0) == 3 * slot(1, 100, 100, 64, 128)      # auto: 16 heads / 16 chunks
+    assert hb(4, 16, 100, 100, 64, 128, 0) == 3 * slot(4, 100, 100, 64, 128)      # 64 heads / 16 chunks
     assert hb(2, 3, 64, 96, 32, 64, 5) == 3 * slot(3, 64, 96, 32, 64)             # capped at H
     assert hb(1, 0, 64, 64, 64, 128, 0) == 0
     fh = lambda q=FAKE, out=FAKE, ws=ctypes.c_void_p(0x10000), wsb=1 << 30, d=64, dv=128, chunk=0, B=1: \

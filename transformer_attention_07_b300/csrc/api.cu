@@ -36,6 +36,25 @@ int check_scalars(float lambda, float lambda_init, float eps) {
 // every byte stride below 2^40.
 bool fits_tensor_map(int64_t H, int64_t N, int64_t W) { return H * N * W * 2 < (int64_t(1) << 40); }
 
+// Checks shared by every prefill entry point, then the launch.  Optional
+// outputs (o_prenorm, o2, lse) and inputs (gamma, qk_scale) may be null.
+int prefill(const diffattn::PrefillArgs& a, void* stream) {
+    if (!a.q1 || !a.k1 || !a.q2 || !a.k2 || !a.v || !a.out) return DIFFATTN_ERR_INVALID_ARG;
+    if (a.B < 0 || a.H < 0 || a.Nq < 0 || a.Nk < 1 || a.d < 1 || a.dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (a.causal != 0 && a.causal != 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (a.causal && a.Nq > a.Nk) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_scalars(a.lambda, a.lambda_init, a.eps)) return s;
+    if (!supported_widths(a.d, a.dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(a.q1) || !aligned16(a.k1) || !aligned16(a.q2) || !aligned16(a.k2) || !aligned16(a.v) ||
+        !aligned16(a.out) || !aligned16(a.o_prenorm) || !aligned16(a.o2) || !aligned4(a.lse) ||
+        !aligned4(a.gamma) || !aligned4(a.qk_scale))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (a.B > 65535 || a.H > 65535) return DIFFATTN_ERR_INVALID_ARG;   // grid y/z limits
+    if (!fits_tensor_map(a.H, a.Nq, a.d) || !fits_tensor_map(a.H, a.Nk, a.dv)) return DIFFATTN_ERR_INVALID_ARG;
+    if ((int64_t)a.B * a.H * a.Nq == 0) return DIFFATTN_OK;
+    return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+}
+
 size_t workspace_for(int B, int H, int dv, int splits) {
     return (size_t)B * (size_t)H * (size_t)splits * 2u * (size_t)(dv + 4) * sizeof(float);
 }
@@ -66,41 +85,18 @@ extern "C" {
 int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
                     float lambda, float lambda_init, int causal, int B, int H, int Nq, int Nk, int d, int dv,
                     const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream) {
-    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID_ARG;
-    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
-    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
-    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
-    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
-    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
-        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma))
-        return DIFFATTN_ERR_INVALID_ARG;
-    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;   // grid y/z limits
-    if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
-    if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
     diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
                             gn_gamma, out, o_prenorm, nullptr, nullptr, nullptr};
-    return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+    return prefill(a, stream);
 }
 
 int diffattn_fwd_fp8(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
                      const float* qk_scale, float lambda, float lambda_init, int causal, int B, int H, int Nq, int Nk,
                      int d, int dv, const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream) {
-    if (!q1 || !k1 || !q2 || !k2 || !v || !qk_scale || !out) return DIFFATTN_ERR_INVALID_ARG;
-    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
-    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
-    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
-    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
-    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
-        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma) || !aligned4(qk_scale))
-        return DIFFATTN_ERR_INVALID_ARG;
-    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
-    if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
-    if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
+    if (!qk_scale) return DIFFATTN_ERR_INVALID_ARG;
     diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
                             gn_gamma, out, o_prenorm, nullptr, nullptr, qk_scale};
-    return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+    return prefill(a, stream);
 }
 
 int diffattn_fwd_train(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
@@ -108,23 +104,9 @@ int diffattn_fwd_train(const void* q1, const void* k1, const void* q2, const voi
                        const float* gn_gamma, float eps, void* out, float* o_prenorm, float* o2, float* lse,
                        void* stream) {
     if (!o_prenorm || !o2 || !lse) return DIFFATTN_ERR_INVALID_ARG;
-    if (!aligned16(o2) || !aligned4(lse)) return DIFFATTN_ERR_INVALID_ARG;
-    // Every other check is that of the inference entry point.
-    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID_ARG;
-    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
-    if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
-    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
-    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
-    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
-    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
-        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma))
-        return DIFFATTN_ERR_INVALID_ARG;
-    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
-    if (!fits_tensor_map(H, Nq, d) || !fits_tensor_map(H, Nk, dv)) return DIFFATTN_ERR_INVALID_ARG;
-    if ((int64_t)B * H * Nq == 0) return DIFFATTN_OK;
     diffattn::PrefillArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, causal, B, H, Nq, Nk, d, dv,
                             gn_gamma, out, o_prenorm, o2, lse, nullptr};
-    return from_launch(diffattn::launch_prefill(a, static_cast<cudaStream_t>(stream)));
+    return prefill(a, stream);
 }
 
 size_t diffattn_bwd_workspace_bytes(int B, int H, int Nq, int dv) {

@@ -158,8 +158,7 @@ size_t diffattn_bwd_workspace_bytes(int B, int H, int Nq, int dv);
  *   NULL when not wanted; dlambda sums over every (b, h, i).
  * workspace: >= diffattn_bwd_workspace_bytes(B, H, Nq, dv) bytes, 256-byte
  *   aligned, no initialisation needed; concurrent calls need separate ones.
- * Supported widths: (d, dv) = (64, 128).  Other widths return
- * DIFFATTN_ERR_UNSUPPORTED.  Nq = 0 writes zero key gradients (the
+ * Supported widths: (d, dv) = (64, 128) or (32, 64), as for the forward.  Nq = 0 writes zero key gradients (the
  * query-side pointers may then be NULL).  Results are
  * deterministic: no atomics, fixed summation orders.
  */

@@ -67,7 +67,7 @@ def _load():
         lib.oracle_diffattn_maps.restype = i32
         lib.oracle_diffattn_bwd.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, f64, f64, i32,
                                             i32, i32, i32, i32, i32, i32, vp, f64,
-                                            vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, i32]
+                                            vp, i64, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, i32]
         lib.oracle_diffattn_bwd.restype = i32
         _lib = lib
     return _lib
@@ -152,7 +152,8 @@ def diffattn_bwd(q1, k1, q2, k2, v, dy, lam, lam_init, causal=False, gamma=None,
     keys whose dk, dv are computed (the same indices for every (b,h)).
     Returns a dict of float64 arrays: dq1, dq2 [B,H,R,d]; dk1, dk2 [B,H,K,d];
     dv [B,H,K,dv]; and, only when neither rows nor keys is given, dlambda
-    (a float) and dgamma [H*dv].
+    (a float), dlambda_rss (the root-sum-square of dlambda's per-row terms,
+    the scale of its rounding error) and dgamma [H*dv].
     """
     arrs = [_as_input(t) for t in (q1, k1, q2, k2, v)]
     types = {t for _, t in arrs}
@@ -177,16 +178,18 @@ def diffattn_bwd(q1, k1, q2, k2, v, dy, lam, lam_init, causal=False, gamma=None,
     out = {"dq1": np.empty((B, H, R, d)), "dq2": np.empty((B, H, R, d)), "dk1": np.empty((B, H, K, d)),
            "dk2": np.empty((B, H, K, d)), "dv": np.empty((B, H, K, dv))}
     dlam = np.zeros(1) if full else None
+    dlam_rss = np.zeros(1) if full else None
     dgam = np.empty(H * dv) if full else None
     rc = _load().oracle_diffattn_bwd(
         _ptr(aq1), _ptr(ak1), _ptr(aq2), _ptr(ak2), _ptr(av), in_type, _ptr(ady), dy_type,
         float(lam), float(lam_init), int(bool(causal)), B, H, Nq, Nk, d, dv, _ptr(g), float(eps),
         _ptr(r), R, _ptr(k), K, _ptr(out["dq1"]), _ptr(out["dq2"]), _ptr(out["dk1"]), _ptr(out["dk2"]),
-        _ptr(out["dv"]), _ptr(dlam), _ptr(dgam), int(threads))
+        _ptr(out["dv"]), _ptr(dlam), _ptr(dgam), _ptr(dlam_rss), int(threads))
     if rc != 0:
         raise ValueError("oracle_diffattn_bwd rejected its arguments")
     if full:
         out["dlambda"] = float(dlam[0])
+        out["dlambda_rss"] = float(dlam_rss[0])
         out["dgamma"] = dgam
     return out
 

@@ -312,7 +312,10 @@ int oracle_diffattn_maps(const void* q1, const void* k1, const void* q2, const v
 //  * dk1, dk2 [B,H,K,d] and dv [B,H,K,dv] for the keys `keys` (K = n_keys;
 //    all keys when keys is null);
 //  * dlambda (one value) and dgamma [H*dv], which sum over every row: they
-//    may be non-null only when rows and keys are both null.
+//    may be non-null only when rows and keys are both null;
+//  * dlambda_rss (one value, same condition): the root-sum-square of the
+//    per-row terms of dlambda, the scale of its rounding error (the terms
+//    cancel, so the sum itself can be much smaller than its terms).
 // Any output may be null.  Only the query rows that are requested, or that
 // see a requested key, are visited.  Returns 0, or 1 on an invalid argument.
 int oracle_diffattn_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
@@ -322,10 +325,10 @@ int oracle_diffattn_bwd(const void* q1, const void* k1, const void* q2, const vo
                         const double* gamma, double eps,
                         const int64_t* rows, int64_t n_rows, const int64_t* keys, int64_t n_keys,
                         double* dq1, double* dq2, double* dk1, double* dk2, double* dv_out,
-                        double* dlambda, double* dgamma, int threads) {
+                        double* dlambda, double* dgamma, double* dlambda_rss, int threads) {
     Problem p{q1, k1, q2, k2, v, in_type, lambda, lambda_init, causal, B, H, Nq, Nk, d, dv, gamma, eps};
     if (check(p) || !dy || dy_type < IN_F64 || dy_type > IN_BF16) return 1;
-    if ((rows || keys) && (dlambda || dgamma)) return 1;
+    if ((rows || keys) && (dlambda || dgamma || dlambda_rss)) return 1;
     const int64_t R = rows ? n_rows : (int64_t)Nq;
     const int64_t K = keys ? n_keys : (int64_t)Nk;
     // Position of each query row / key in the outputs (-1: not requested).
@@ -344,7 +347,7 @@ int oracle_diffattn_bwd(const void* q1, const void* k1, const void* q2, const vo
     }
     const double inv_sqrt_d = 1.0 / std::sqrt((double)d);
     const int64_t BH = (int64_t)B * H;
-    std::vector<double> dlam_bh(BH, 0.0), dgam_bh(dgamma ? BH * dv : 0, 0.0);
+    std::vector<double> dlam_bh(BH, 0.0), dlam_sq_bh(BH, 0.0), dgam_bh(dgamma ? BH * dv : 0, 0.0);
     if (dq1) std::fill(dq1, dq1 + BH * R * d, 0.0);
     if (dq2) std::fill(dq2, dq2 + BH * R * d, 0.0);
     if (dk1) std::fill(dk1, dk1 + BH * K * d, 0.0);
@@ -358,8 +361,10 @@ int oracle_diffattn_bwd(const void* q1, const void* k1, const void* q2, const vo
         for (int64_t i = 0; i < Nq; ++i) {
             const bool want_row = row_slot[i] >= 0;
             const bool sees_key = visible_keys(p, i) > min_key;
-            if (!want_row && !sees_key && !dlambda && !dgamma) continue;
-            dlam_bh[bh] += row_backward(p, dy, dy_type, b, h, i, w, dgamma ? &dgam_bh[bh * dv] : nullptr);
+            if (!want_row && !sees_key && !dlambda && !dgamma && !dlambda_rss) continue;
+            const double term = row_backward(p, dy, dy_type, b, h, i, w, dgamma ? &dgam_bh[bh * dv] : nullptr);
+            dlam_bh[bh] += term;
+            dlam_sq_bh[bh] += term * term;
             const int64_t n = (int64_t)w.ds1.size();
             if (want_row) {
                 const int64_t o = (bh * R + row_slot[i]) * d;
@@ -389,6 +394,11 @@ int oracle_diffattn_bwd(const void* q1, const void* k1, const void* q2, const vo
         double s = 0.0;
         for (int64_t bh = 0; bh < BH; ++bh) s += dlam_bh[bh];
         *dlambda = s;
+    }
+    if (dlambda_rss) {
+        double s = 0.0;
+        for (int64_t bh = 0; bh < BH; ++bh) s += dlam_sq_bh[bh];
+        *dlambda_rss = std::sqrt(s);
     }
     if (dgamma) {
         std::fill(dgamma, dgamma + (int64_t)H * dv, 0.0);

@@ -10,10 +10,13 @@ term; over sums of many terms they partly cancel.  The checks are therefore
 relative to the size of each gradient tensor: the Frobenius-norm relative
 error must stay below 1e-2 and the largest element error below 3e-2 of the
 tensor's largest magnitude (plus an absolute 1e-5 per element, for
-gradients that vanish exactly); dlambda (one fp32 sum over every row) within
-1e-2 relative plus 1e-4 per square root of the row count (with one key per
-row the normalisation makes y independent of lambda and dlambda is 0 up to
-rounding).
+gradients that vanish exactly).  dlambda is a sum of one term per row that
+can cancel to far below its terms (with one key per row the normalisation
+makes y independent of lambda and dlambda is 0); each term carries the
+forward output's rounding (about 1e-3 relative, through the GroupNorm
+statistics and A2 V), with independent signs, so the error scales with the
+root-sum-square of the terms: within 1e-2 of dlambda plus 3e-3 of that
+root-sum-square, which the oracle reports.
 """
 import numpy as np
 import pytest
@@ -65,20 +68,23 @@ def cpu(*ts):
     return [t.cpu() for t in ts]
 
 
-@pytest.mark.parametrize("B,H,Nq,Nk,causal,lam", [
-    (2, 2, 256, 256, True, 0.5),
-    (1, 2, 200, 333, True, 0.8),
-    (1, 2, 200, 333, False, -0.3),
-    (2, 1, 130, 70, False, 0.0),
-    (1, 1, 1, 1, True, 0.6),
+@pytest.mark.parametrize("B,H,Nq,Nk,causal,lam,d,dv", [
+    (2, 2, 256, 256, True, 0.5, 64, 128),
+    (1, 2, 200, 333, True, 0.8, 64, 128),
+    (1, 2, 200, 333, False, -0.3, 64, 128),
+    (2, 1, 130, 70, False, 0.0, 64, 128),
+    (1, 1, 1, 1, True, 0.6, 64, 128),
+    (2, 2, 256, 256, True, 0.5, 32, 64),
+    (1, 2, 200, 333, True, 0.8, 32, 64),
+    (2, 1, 130, 70, False, -0.3, 32, 64),
 ])
-def test_backward_matches_oracle(B, H, Nq, Nk, causal, lam):
-    q1, k1, q2, k2, v, dy, gamma = inputs(B, H, Nq, Nk, seed=Nq + Nk + int(causal))
+def test_backward_matches_oracle(B, H, Nq, Nk, causal, lam, d, dv):
+    q1, k1, q2, k2, v, dy, gamma = inputs(B, H, Nq, Nk, seed=Nq + Nk + int(causal) + d, d=d, dv=dv)
     _, _, g = run(q1, k1, q2, k2, v, dy, gamma, lam, 0.8, causal)
     ref = oracle.diffattn_bwd(*cpu(q1, k1, q2, k2, v, dy), lam, 0.8, causal=causal, gamma=gamma.double().cpu())
     for n in ("dq1", "dk1", "dq2", "dk2", "dv"):
         rel_check(n, g[n].float().cpu().numpy(), ref[n])
-    assert abs(g["dlambda"].item() - ref["dlambda"]) <= 1e-2 * abs(ref["dlambda"]) + 1e-4 * np.sqrt(B * H * Nq)
+    assert abs(g["dlambda"].item() - ref["dlambda"]) <= 1e-2 * abs(ref["dlambda"]) + 3e-3 * ref["dlambda_rss"]
     rel_check("dgamma", g["dgamma"].cpu().numpy(), ref["dgamma"])
 
 

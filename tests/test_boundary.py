@@ -146,7 +146,7 @@ def test_bwd_validation(lib):
     assert bwd(grad=None) == INVALID
     assert bwd(Nk=0) == INVALID
     assert bwd(causal=1, Nq=5, Nk=4) == INVALID
-    assert bwd(d=32, dv=64) == UNSUPPORTED
+    assert bwd(d=32, dv=128) == UNSUPPORTED
     assert bwd(q=MISALIGNED) == INVALID
     assert bwd(dl=ctypes.c_void_p(0x10002)) == INVALID
     assert bwd(ws=None) == WORKSPACE

@@ -116,6 +116,21 @@ def test_row_and_key_subsets_equal_the_full_result():
     assert "dlambda" not in sub and "dgamma" not in sub
 
 
+def test_dlambda_rss_is_the_root_sum_square_of_row_terms():
+    """dlambda sums one term per row; computing each row alone (a one-row
+    problem per query, through the full oracle) gives the terms."""
+    t, dy, gamma = problem(1, 1, 6, 6, 4, 8, seed=11)
+    full = oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, 0.7, 0.8, gamma=gamma)
+    terms = []
+    for i in range(6):
+        dyi = np.zeros_like(dy)
+        dyi[:, :, i] = dy[:, :, i]
+        terms.append(oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dyi, 0.7, 0.8,
+                                         gamma=gamma)["dlambda"])
+    assert abs(sum(terms) - full["dlambda"]) < 1e-12
+    assert abs(np.sqrt(np.sum(np.square(terms))) - full["dlambda_rss"]) < 1e-12
+
+
 def test_gradients_vanish_when_lambda_init_is_one():
     """With lambda_init = 1 the output scale (1 - lambda_init) is 0, so y = 0 for
     every input and every gradient is exactly 0."""

@@ -127,7 +127,7 @@ int diffattn_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
     if (causal != 0 && causal != 1) return DIFFATTN_ERR_INVALID_ARG;
     if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
     if (int s = check_scalars(lambda, lambda_init, eps)) return s;
-    if (!(d == 64 && dv == 128)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
     if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
         !aligned16(dy) || !aligned16(o_prenorm) || !aligned16(o2) || !aligned4(lse) || !aligned4(gn_gamma) ||
         !aligned16(dq1) || !aligned16(dk1) || !aligned16(dq2) || !aligned16(dk2) || !aligned16(dv_grad) ||

@@ -259,13 +259,20 @@ struct BwdDqLayout {
     static constexpr int NBAR = B_DQFULL + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
     static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
-    static constexpr uint32_t SMEM_BYTES = USED + 1024;
+    // +1024 for aligning the dynamic base; at least 120 KB so that a single
+    // CTA (which takes all 512 TMEM columns) is resident per SM.
+    static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u) ? USED + 1024 : 120u * 1024u;
     // Tensor memory: S1, S2, dP (128 columns each; dS_r in bf16 is written
     // over the first 64 columns of S_r), then the two dQ accumulators.
-    static constexpr uint32_t TM_S1 = 0, TM_S2 = 128, TM_DP = 256, TM_DQ1 = 384, TM_DQ2 = 448;
+    static constexpr uint32_t TM_S1 = 0, TM_S2 = 128, TM_DP = 256, TM_DQ1 = 384, TM_DQ2 = 384 + D;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 320;
-    static_assert(D == 64 && DV == 128, "backward widths");
+    // Q/K rows are one swizzle span wide (128 or 64 bytes); dO and V come in
+    // 64-column boxes of 128-byte rows.
+    static constexpr uint32_t QK_ROW = D * 2;
+    static constexpr uint32_t QK_SWZ = QK_ROW == 128 ? SWZ_128B : SWZ_64B;
+    static constexpr uint32_t QK_SBO = 8 * QK_ROW;
+    static_assert((D == 64 && DV == 128) || (D == 32 && DV == 64), "backward widths");
     static_assert(SMEM_BYTES <= 227u * 1024u && SMEM_BYTES > 114u * 1024u, "one CTA per SM");
 };
 
@@ -361,11 +368,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             constexpr uint32_t idesc_dq = idesc_bf16_f32(L::BM, D, true);       // dQ: K tile MN-major
             bool ok = mbar_wait(bar(L::B_Q), 0, ERR_SITE_BWD_MMA);
             tc_fence_after();
-            const uint64_t dq1 = smem_desc(sb + L::OFF_Q1, 16, 1024, SWZ_128B);
-            const uint64_t dq2 = smem_desc(sb + L::OFF_Q2, 16, 1024, SWZ_128B);
+            const uint64_t dq1 = smem_desc(sb + L::OFF_Q1, 16, L::QK_SBO, L::QK_SWZ);
+            const uint64_t dq2 = smem_desc(sb + L::OFF_Q2, 16, L::QK_SBO, L::QK_SWZ);
             const uint64_t ddo = smem_desc(sb + L::OFF_DO, 16, 1024, SWZ_128B);
-            const uint64_t dk0 = smem_desc(sb + L::OFF_K, 16, 1024, SWZ_128B);                   // K1, stage 0
-            const uint64_t dkm0 = smem_desc(sb + L::OFF_K, L::K_BYTES, 1024, SWZ_128B);          // K1 as MN-major B
+            const uint64_t dk0 = smem_desc(sb + L::OFF_K, 16, L::QK_SBO, L::QK_SWZ);                 // K1, stage 0
+            const uint64_t dkm0 = smem_desc(sb + L::OFF_K, L::K_BYTES, L::QK_SBO, L::QK_SWZ);        // K1 as MN-major B
             const uint64_t dv0 = smem_desc(sb + L::OFF_K + 2 * L::K_BYTES, 16, 1024, SWZ_128B);  // V, stage 0
             constexpr uint64_t STAGE16 = L::STAGE >> 4, K2OFF = L::K_BYTES >> 4;
             // dP = dO V^T: k over dv, two 64-column boxes of each operand.
@@ -389,7 +396,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 #pragma unroll
                 for (int k = 0; k < L::BN / 16; ++k)
                     mma_ts(tmem + (r ? L::TM_DQ2 : L::TM_DQ1), tmem + (r ? L::TM_S2 : L::TM_S1) + 8u * k,
-                           dkm0 + so + (r ? K2OFF : 0) + (uint64_t)(k * (16 * 128 >> 4)), idesc_dq,
+                           dkm0 + so + (r ? K2OFF : 0) + (uint64_t)(k * (16 * L::QK_ROW >> 4)), idesc_dq,
                            (!first || k > 0) ? 1u : 0u);
             };
             if (ok) ok = mbar_wait(bar(L::B_KFULL + 0), 0, ERR_SITE_BWD_MMA);
@@ -489,8 +496,11 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         mbar_wait(bar(L::B_DQFULL), 0, ERR_SITE_BWD_EPILOGUE);
         __syncwarp();
         tc_fence_after();
-        uint32_t a[64];
-        tmem_ld64(tmem + t_lane + (r ? L::TM_DQ2 : L::TM_DQ1), a);
+        uint32_t a[D];
+        if constexpr (D == 64)
+            tmem_ld64(tmem + t_lane + (r ? L::TM_DQ2 : L::TM_DQ1), a);
+        else
+            tmem_ld32(tmem + t_lane + (r ? L::TM_DQ2 : L::TM_DQ1), a);
         if (qi < p.Nq) {
             uint4* dst = reinterpret_cast<uint4*>((r ? p.dq2 : p.dq1) + (bh * p.Nq + qi) * D);
 #pragma unroll
@@ -543,17 +553,24 @@ struct BwdDkvLayout {
     static constexpr int NBAR = B_DONE + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
     static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
-    static constexpr uint32_t SMEM_BYTES = USED + 1024;
+    // +1024 for aligning the dynamic base; at least 120 KB so that a single
+    // CTA (which takes all 512 TMEM columns) is resident per SM.
+    static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u) ? USED + 1024 : 120u * 1024u;
     // Tensor memory: for each half of the query tile (32 queries), S1^T,
     // S2^T, dP^T (32 columns each; dS1^T, dS2^T and (A1 - lambda A2)^T in
     // bf16 are written over their first 16), then the dV, dK1, dK2
     // accumulators.
     static constexpr int HQ = BQ / 2;                  // queries per half
     static constexpr uint32_t TM_HALF = 96, TM_S1 = 0, TM_S2 = 32, TM_DP = 64;
-    static constexpr uint32_t TM_DV = 256, TM_DK1 = 384, TM_DK2 = 448;
+    static constexpr uint32_t TM_DV = 256, TM_DK1 = 256 + DV, TM_DK2 = 256 + DV + D;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 320;
-    static_assert(D == 64 && DV == 128, "backward widths");
+    // Q/K rows are one swizzle span wide (128 or 64 bytes); dO and V come in
+    // 64-column boxes of 128-byte rows.
+    static constexpr uint32_t QK_ROW = D * 2;
+    static constexpr uint32_t QK_SWZ = QK_ROW == 128 ? SWZ_128B : SWZ_64B;
+    static constexpr uint32_t QK_SBO = 8 * QK_ROW;
+    static_assert((D == 64 && DV == 128) || (D == 32 && DV == 64), "backward widths");
     static_assert(STAGE % 1024 == 0 && RC_BYTES <= 1024, "stage layout");
     static_assert(SMEM_BYTES <= 227u * 1024u && SMEM_BYTES > 114u * 1024u, "one CTA per SM");
 };
@@ -652,15 +669,16 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             constexpr uint32_t idesc_dk = idesc_bf16_f32(L::BK, D, true);       // dK: Q MN-major
             bool ok = mbar_wait(bar(L::B_KV), 0, ERR_SITE_BWD_MMA);
             tc_fence_after();
-            const uint64_t dk1 = smem_desc(sb + L::OFF_K1, 16, 1024, SWZ_128B);
-            const uint64_t dk2 = smem_desc(sb + L::OFF_K2, 16, 1024, SWZ_128B);
+            const uint64_t dk1 = smem_desc(sb + L::OFF_K1, 16, L::QK_SBO, L::QK_SWZ);
+            const uint64_t dk2 = smem_desc(sb + L::OFF_K2, 16, L::QK_SBO, L::QK_SWZ);
             const uint64_t dvv = smem_desc(sb + L::OFF_V, 16, 1024, SWZ_128B);
-            const uint64_t dq0 = smem_desc(sb + L::OFF_Q, 16, 1024, SWZ_128B);                 // Q1 (K-major), stage 0
-            const uint64_t dqm0 = smem_desc(sb + L::OFF_Q, L::Q_BYTES, 1024, SWZ_128B);        // Q1 as MN-major B
+            const uint64_t dq0 = smem_desc(sb + L::OFF_Q, 16, L::QK_SBO, L::QK_SWZ);              // Q1 (K-major), stage 0
+            const uint64_t dqm0 = smem_desc(sb + L::OFF_Q, L::Q_BYTES, L::QK_SBO, L::QK_SWZ);     // Q1 as MN-major B
             const uint64_t ddo0 = smem_desc(sb + L::OFF_Q + L::ST_DO, 16, 1024, SWZ_128B);     // dO (K-major)
             const uint64_t ddom0 = smem_desc(sb + L::OFF_Q + L::ST_DO, L::DO_BOX, 1024, SWZ_128B);   // dO MN-major
             constexpr uint64_t STAGE16 = L::STAGE >> 4, Q2OFF = L::ST_Q2 >> 4;
-            constexpr uint64_t HALF16 = (L::HQ * 128) >> 4;   // 32 rows of a 128-byte-wide tile
+            // 32 rows of the Q tiles and of the (128-byte-row) dO boxes
+            constexpr uint64_t QHALF16 = (L::HQ * L::QK_ROW) >> 4, DOHALF16 = (L::HQ * 128) >> 4;
             // The two halves of each query tile alternate: while the dS warps
             // of one half work, the tensor core runs the other half's
             // gradients and next scores.
@@ -678,35 +696,37 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                         // Gradients of the previous tile's half hh: A operands
                         // are the bf16 tiles the dS warps wrote over its scores.
                         const int tp = t - 1;
-                        const uint64_t so = (uint64_t)(tp % L::QST) * STAGE16 + (uint64_t)hh * HALF16;
+                        const uint64_t st = (uint64_t)(tp % L::QST) * STAGE16;
+                        const uint64_t sq = st + (uint64_t)hh * QHALF16, sd = st + (uint64_t)hh * DOHALF16;
                         ok = mbar_wait(bar(L::B_PFULL + hh), tp & 1, ERR_SITE_BWD_MMA);
                         if (!ok) break;
                         tc_fence_after();
 #pragma unroll
                         for (int k = 0; k < L::HQ / 16; ++k) {
-                            const uint64_t ko = (uint64_t)(k * (16 * 128 >> 4));
+                            const uint64_t kd = (uint64_t)(k * (16 * 128 >> 4)), kq = (uint64_t)(k * (16 * L::QK_ROW >> 4));
                             const uint32_t acc = (tp > 0 || hh > 0 || k > 0) ? 1u : 0u;
-                            mma_ts(tmem + L::TM_DV, th + L::TM_DP + 8u * k, ddom0 + so + ko, idesc_dv, acc);
-                            mma_ts(tmem + L::TM_DK1, th + L::TM_S1 + 8u * k, dqm0 + so + ko, idesc_dk, acc);
-                            mma_ts(tmem + L::TM_DK2, th + L::TM_S2 + 8u * k, dqm0 + so + Q2OFF + ko, idesc_dk, acc);
+                            mma_ts(tmem + L::TM_DV, th + L::TM_DP + 8u * k, ddom0 + sd + kd, idesc_dv, acc);
+                            mma_ts(tmem + L::TM_DK1, th + L::TM_S1 + 8u * k, dqm0 + sq + kq, idesc_dk, acc);
+                            mma_ts(tmem + L::TM_DK2, th + L::TM_S2 + 8u * k, dqm0 + sq + Q2OFF + kq, idesc_dk, acc);
                         }
                         if (hh == 1) mma_commit(bar(L::B_QEMPTY + tp % L::QST));
                     }
                     if (t < n_t) {
-                        const uint64_t so = (uint64_t)qs * STAGE16 + (uint64_t)hh * HALF16;
+                        const uint64_t st = (uint64_t)qs * STAGE16;
+                        const uint64_t sq = st + (uint64_t)hh * QHALF16, sd = st + (uint64_t)hh * DOHALF16;
                         // dP^T = V dO^T: k over dv, two 64-column boxes of each operand.
 #pragma unroll
                         for (int k = 0; k < DV / 16; ++k)
                             mma_ss(th + L::TM_DP, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
-                                   ddo0 + so + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
+                                   ddo0 + sd + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
                                    k > 0 ? 1u : 0u);
 #pragma unroll
                         for (int k = 0; k < D / 16; ++k)
-                            mma_ss(th + L::TM_S1, dk1 + (uint64_t)(2 * k), dq0 + so + (uint64_t)(2 * k), idesc_s,
+                            mma_ss(th + L::TM_S1, dk1 + (uint64_t)(2 * k), dq0 + sq + (uint64_t)(2 * k), idesc_s,
                                    k > 0 ? 1u : 0u);
 #pragma unroll
                         for (int k = 0; k < D / 16; ++k)
-                            mma_ss(th + L::TM_S2, dk2 + (uint64_t)(2 * k), dq0 + so + Q2OFF + (uint64_t)(2 * k),
+                            mma_ss(th + L::TM_S2, dk2 + (uint64_t)(2 * k), dq0 + sq + Q2OFF + (uint64_t)(2 * k),
                                    idesc_s, k > 0 ? 1u : 0u);
                         mma_commit(bar(L::B_SFULL + hh));
                     }
@@ -775,13 +795,13 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         __syncwarp();
         tc_fence_after();
         const bool store = kj < p.Nk;
-        // dV: columns [64 hf, 64 hf + 64).
+        // dV: columns [dv/2 hf, dv/2 (hf + 1)).
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < DV / 64; ++c) {
             uint32_t a[32];
-            tmem_ld32(tmem + t_lane + L::TM_DV + 64 * hf + 32 * c, a);
+            tmem_ld32(tmem + t_lane + L::TM_DV + (DV / 2) * hf + 32 * c, a);
             if (store) {
-                uint4* dst = reinterpret_cast<uint4*>(p.dv + (bh * p.Nk + kj) * DV + 64 * hf + 32 * c);
+                uint4* dst = reinterpret_cast<uint4*>(p.dv + (bh * p.Nk + kj) * DV + (DV / 2) * hf + 32 * c);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     dst[i] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * i]), __uint_as_float(a[8 * i + 1])),
@@ -790,16 +810,19 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                                         pack_bf16x2(__uint_as_float(a[8 * i + 6]), __uint_as_float(a[8 * i + 7])));
             }
         }
-        // dK1, dK2: columns [32 hf, 32 hf + 32), times 1/sqrt(d).
+        // dK1, dK2: columns [d/2 hf, d/2 (hf + 1)), times 1/sqrt(d).
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
-            uint32_t a[32];
-            tmem_ld32(tmem + t_lane + (r ? L::TM_DK2 : L::TM_DK1) + 32 * hf, a);
+            uint32_t a[D / 2];
+            if constexpr (D == 64)
+                tmem_ld32(tmem + t_lane + (r ? L::TM_DK2 : L::TM_DK1) + (D / 2) * hf, a);
+            else
+                tmem_ld16(tmem + t_lane + (r ? L::TM_DK2 : L::TM_DK1) + (D / 2) * hf, a);
             if (store) {
-                uint4* dst = reinterpret_cast<uint4*>((r ? p.dk2 : p.dk1) + (bh * p.Nk + kj) * D + 32 * hf);
+                uint4* dst = reinterpret_cast<uint4*>((r ? p.dk2 : p.dk1) + (bh * p.Nk + kj) * D + (D / 2) * hf);
                 const float s = p.scale;
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < D / 16; ++i)
                     dst[i] = make_uint4(
                         pack_bf16x2(__uint_as_float(a[8 * i]) * s, __uint_as_float(a[8 * i + 1]) * s),
                         pack_bf16x2(__uint_as_float(a[8 * i + 2]) * s, __uint_as_float(a[8 * i + 3]) * s),

@@ -195,20 +195,22 @@ static int launch_backward_t(const BwdArgs& a, cudaStream_t st) {
     bwd_prep_kernel<DV><<<dim3(w.nchunk, a.H, a.B), 256, 0, st>>>(p);
     if (!cuda_ok(cudaGetLastError(), "backward: prep launch")) return LAUNCH_ERR_CUDA;
 
-    CUtensorMap q1a, q2a, doa, k1a, k2a, va;   // dQ sweep: 128-row Q/dO boxes, 64-row K/V boxes
+    CUtensorMap q1a, q2a, doa, k1a, k2a, va;   // dQ sweep: 128-row Q/dO boxes, BN-row K/V boxes
     CUtensorMap q1b, q2b, dob, k1b, k2b, vb;   // dK/dV sweep: 64-row Q/dO boxes, 128-row K/V boxes
     const auto S = CU_TENSOR_MAP_SWIZZLE_128B;
-    if (!make_map_bhnd(&q1a, a.q1, a.B, a.H, a.Nq, D, 64, LQ::BM, S) ||
-        !make_map_bhnd(&q2a, a.q2, a.B, a.H, a.Nq, D, 64, LQ::BM, S) ||
+    // Q/K rows are one swizzle span wide: 128 bytes (d = 64) or 64 bytes (d = 32).
+    const auto SQ = D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!make_map_bhnd(&q1a, a.q1, a.B, a.H, a.Nq, D, D, LQ::BM, SQ) ||
+        !make_map_bhnd(&q2a, a.q2, a.B, a.H, a.Nq, D, D, LQ::BM, SQ) ||
         !make_map_bhnd(&doa, p.dout, a.B, a.H, a.Nq, DV, 64, LQ::BM, S) ||
-        !make_map_bhnd(&k1a, a.k1, a.B, a.H, a.Nk, D, 64, LQ::BN, S) ||
-        !make_map_bhnd(&k2a, a.k2, a.B, a.H, a.Nk, D, 64, LQ::BN, S) ||
+        !make_map_bhnd(&k1a, a.k1, a.B, a.H, a.Nk, D, D, LQ::BN, SQ) ||
+        !make_map_bhnd(&k2a, a.k2, a.B, a.H, a.Nk, D, D, LQ::BN, SQ) ||
         !make_map_bhnd(&va, a.v, a.B, a.H, a.Nk, DV, 64, LQ::BN, S) ||
-        !make_map_bhnd(&q1b, a.q1, a.B, a.H, a.Nq, D, 64, LK::BQ, S) ||
-        !make_map_bhnd(&q2b, a.q2, a.B, a.H, a.Nq, D, 64, LK::BQ, S) ||
+        !make_map_bhnd(&q1b, a.q1, a.B, a.H, a.Nq, D, D, LK::BQ, SQ) ||
+        !make_map_bhnd(&q2b, a.q2, a.B, a.H, a.Nq, D, D, LK::BQ, SQ) ||
         !make_map_bhnd(&dob, p.dout, a.B, a.H, a.Nq, DV, 64, LK::BQ, S) ||
-        !make_map_bhnd(&k1b, a.k1, a.B, a.H, a.Nk, D, 64, LK::BK, S) ||
-        !make_map_bhnd(&k2b, a.k2, a.B, a.H, a.Nk, D, 64, LK::BK, S) ||
+        !make_map_bhnd(&k1b, a.k1, a.B, a.H, a.Nk, D, D, LK::BK, SQ) ||
+        !make_map_bhnd(&k2b, a.k2, a.B, a.H, a.Nk, D, D, LK::BK, SQ) ||
         !make_map_bhnd(&vb, a.v, a.B, a.H, a.Nk, DV, 64, LK::BK, S))
         return LAUNCH_ERR_CUDA;
 
@@ -238,6 +240,8 @@ static int launch_backward_t(const BwdArgs& a, cudaStream_t st) {
 int launch_backward(const BwdArgs& a, cudaStream_t st) {
     if (a.d == 64 && a.dv == 128)
         return a.causal ? launch_backward_t<64, 128, true>(a, st) : launch_backward_t<64, 128, false>(a, st);
+    if (a.d == 32 && a.dv == 64)
+        return a.causal ? launch_backward_t<32, 64, true>(a, st) : launch_backward_t<32, 64, false>(a, st);
     return LAUNCH_ERR_UNSUPPORTED;
 }
 

@@ -150,6 +150,17 @@ def sample_rows_uniform(N, n, seed):
     return sorted(set(torch.randint(0, N, (n,), generator=g).tolist()))
 
 
+def step_config(wp, wd, do_pre, do_dec, world):
+    """The `config` object of the JSON line (the same for both arms)."""
+    desc = []
+    if do_pre:
+        desc.append(f"{wp.name}: causal DiffAttn prefill B{wp.B} H{wp.H} N{wp.Nq} d{wp.d} dv{wp.dv}")
+    if do_dec:
+        desc.append(f"{wd.name}: split-KV decode B{wd.B} H{wd.H} Nk{wd.Nk} d{wd.d} dv{wd.dv}")
+    return {"workload": " + ".join(desc), "parallelism": f"one independent problem per GPU x{world}",
+            "l2": "inputs larger than L2 (prefill 768 MiB; decode streams 16 GiB per step)"}
+
+
 def run_reference(args, world, rank):
     """The fp64 oracle on the host cores: each step = a bounded row sample."""
     import torch
@@ -172,7 +183,7 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{PREFILL}: causal prefill B1 H16 N65536 d64 dv128", "sample": sample},
+            "config": step_config(w, WORKLOADS[DECODE], True, True, world),
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -506,13 +517,7 @@ def run_cuda(args, world, rank, local):
     line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic"}
-    desc = []
-    if do_pre:
-        desc.append(f"{wp.name}: causal DiffAttn prefill B{wp.B} H{wp.H} N{wp.Nq} d{wp.d} dv{wp.dv}")
-    if do_dec:
-        desc.append(f"{wd.name}: split-KV decode B{wd.B} H{wd.H} Nk{wd.Nk} d{wd.d} dv{wd.dv}")
-    line["config"] = {"workload": " + ".join(desc), "parallelism": f"one independent problem per GPU x{world}",
-                      "l2": "inputs larger than L2 (prefill 768 MiB; decode streams 16 GiB per step)"}
+    line["config"] = step_config(wp, wd, do_pre, do_dec, world)
     if do_dec:
         dec_gbs = wd.kv_bytes * args.steps * world / (dec_ms * 1e-3) / 1e9
         dec_roof = {"bound": "hbm", "achieved": dec_gbs / world, "peak": peak_hbm, "unit": "GB/s",

@@ -18,10 +18,10 @@ import ctypes
 import os
 
 __all__ = [
-    "fwd", "fwd_host", "fwd_host_workspace_bytes", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes", "standard_fwd", "decode", "decode_paged",
-    "decode_workspace_bytes", "decode_partials", "decode_partials_bytes", "decode_merge", "gather_partials",
-    "decode_sharded", "status_string", "last_device_error", "load", "LIB_PATH", "DiffAttnError",
-    "SUPPORTED_WIDTHS",
+    "fwd", "fwd_host", "fwd_host_workspace_bytes", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes",
+    "standard_fwd", "decode", "decode_paged", "decode_workspace_bytes", "decode_partials", "decode_partials_bytes",
+    "decode_merge", "gather_partials", "decode_sharded", "status_string", "last_device_error", "load", "LIB_PATH",
+    "DiffAttnError", "SUPPORTED_WIDTHS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdiffattn.so")

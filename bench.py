@@ -413,7 +413,8 @@ def run_cuda(args, world, rank, local):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     wp, wd = WORKLOADS[args.prefill_workload], WORKLOADS[args.decode_workload]
-    do_pre, do_dec = args.only in ("all", "prefill", "backward"), args.only in ("all", "decode")
+    do_pre = args.only in ("all", "prefill", "backward", "fp8")
+    do_dec = args.only in ("all", "decode")
     # Each rank its own independent problem (seed offset by rank).
     pin = make_inputs(wp, device=dev, seed=rank_seed(wp.seed, rank)) if do_pre else None
     din = make_inputs(wd, device=dev, seed=rank_seed(wd.seed, rank)) if do_dec else None
@@ -422,9 +423,18 @@ def run_cuda(args, world, rank, local):
     ws = torch.empty(da.decode_workspace_bytes(wd.B, wd.H, wd.Nk, wd.dv, 0), dtype=torch.uint8,
                      device=dev) if do_dec else None
     stream = torch.cuda.current_stream(dev)
+    # Profiling modes: one NEXT-row measurement alone (warm-up, then --steps calls).
     if args.only == "backward":
-        # Profiling mode: the backward pass alone (warm-up 2, then --steps calls).
         print(json.dumps({"backward": backward_throughput(dev, wp, pin, reps=args.steps)}), flush=True)
+        return 0
+    if args.only == "fp8":
+        print(json.dumps({"fp8_qk": fp8_throughput(dev, wp, pin, reps=args.steps)}), flush=True)
+        return 0
+    if args.only == "paged":
+        print(json.dumps({"decode_paged": paged_decode_throughput(dev, reps=args.steps)}), flush=True)
+        return 0
+    if args.only == "standard":
+        print(json.dumps({"single_map_baseline": compare_single_map(dev, reps=args.steps)}), flush=True)
         return 0
 
     def prefill():
@@ -578,7 +588,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the DiffAttn vs single-map (standard attention) comparison")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward", "fp8", "paged", "standard"],
+                    default="all",
                     help="run one stage per step (profiling of a single kernel)")
     ap.add_argument("--prefill-workload", default=PREFILL)
     ap.add_argument("--decode-workload", default=DECODE)

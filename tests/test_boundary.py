@@ -129,10 +129,10 @@ def test_fwd_train_validation(lib):
 def test_bwd_workspace_bytes(lib):
     ws = lib.diffattn_bwd_workspace_bytes
     align = lambda x: (x + 255) // 256 * 256
-    # do (bf16) + per-row constants (Nq rounded up to 128) + partial sums per 64 rows
+    # do (bf16) + per-row constants in two layouts (Nq rounded up to 128) + partial sums per 64 rows
     B, H, Nq, dv = 2, 3, 200, 128
     pad = 256
-    assert ws(B, H, Nq, dv) == (align(B * H * Nq * dv * 2) + align(B * H * pad * 16) +
+    assert ws(B, H, Nq, dv) == (align(B * H * Nq * dv * 2) + 2 * align(B * H * pad * 16) +
                                 align(B * H * (pad // 64) * dv * 4) + align(B * H * (pad // 64) * 4))
     assert ws(-1, 1, 1, 128) == 0
 

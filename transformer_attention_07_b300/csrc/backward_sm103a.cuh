@@ -54,6 +54,8 @@ struct BwdParams {
     const float* lse;       // fp32 [2,B,H,Nq]: per-map log-sum-exp (natural log)
     uint16_t* dout;         // bf16 [B,H,Nq,dv]: gradient of the pre-norm output
     float4* rowc;           // [B*H*Nq_pad]: (lse1 log2 e, lse2 log2 e, D1, D2); padding rows (inf, inf, 0, 0)
+    float* rowt;            // [B*H*Nq_pad/128][4][128]: the same constants negated, one row of 128
+                            // per constant and 128-row block (padding rows: -inf, -inf, 0, 0)
     float* gpart;           // [B*H*nchunk, dv]: dgamma partial sums
     float* lpart;           // [B*H*nchunk]: dlambda partial sums
     uint16_t *dq1, *dq2;    // bf16 [B,H,Nq,d]
@@ -148,6 +150,10 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const BwdParams p) {
             rc = make_float4(p.lse[bh * p.Nq + i] * log2e, p.lse[(BH + bh) * p.Nq + i] * log2e, d1, d2);
         }
         if (lane == 0 && i < p.Nq_pad) p.rowc[bh * p.Nq_pad + i] = rc;
+        if (lane < 4 && i < p.Nq_pad) {
+            const float c = lane == 0 ? rc.x : lane == 1 ? rc.y : lane == 2 ? rc.z : rc.w;
+            p.rowt[(bh * p.Nq_pad + (i & ~127)) * 4 + lane * 128 + (i & 127)] = -c;
+        }
     }
     // Block sums of the dgamma and dlambda contributions, warps in order.
     __shared__ float sg_part[8][DV];
@@ -528,8 +534,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 template <int D, int DV>
 struct BwdDkvLayout {
     static constexpr int BK = 128;   // keys per CTA (MMA M)
-    static constexpr int BQ = 64;    // query rows per tile
-    static constexpr int QST = 3;    // ring depth of (Q1, Q2, dO, row constants)
+    static constexpr int BQ = 128;   // query rows per tile (MMA N of the score products)
+    static constexpr int QST = 2;    // ring depth of (Q1, Q2, dO, row constants)
     static constexpr uint32_t K_BYTES = BK * D * 2;
     static constexpr uint32_t V_BOX = BK * 128;
     static constexpr uint32_t V_BYTES = BK * DV * 2;
@@ -537,7 +543,7 @@ struct BwdDkvLayout {
     static constexpr uint32_t DO_BOX = BQ * 128;
     static constexpr uint32_t DO_BYTES = BQ * DV * 2;
     static constexpr uint32_t RC_BYTES = BQ * 16;
-    static constexpr uint32_t STAGE = 2 * Q_BYTES + DO_BYTES + 1024;   // Q1, Q2, dO, row constants
+    static constexpr uint32_t STAGE = 2 * Q_BYTES + DO_BYTES + RC_BYTES;   // Q1, Q2, dO, row constants
     static constexpr uint32_t ST_Q2 = Q_BYTES, ST_DO = 2 * Q_BYTES, ST_RC = 2 * Q_BYTES + DO_BYTES;
     static constexpr uint32_t OFF_K1 = 0;
     static constexpr uint32_t OFF_K2 = K_BYTES;
@@ -547,22 +553,26 @@ struct BwdDkvLayout {
     static constexpr int B_KV = 0;
     static constexpr int B_QFULL = 1;
     static constexpr int B_QEMPTY = B_QFULL + QST;
-    static constexpr int B_SFULL = B_QEMPTY + QST;   // [half]
-    static constexpr int B_PFULL = B_SFULL + 2;      // [half]
-    static constexpr int B_DONE = B_PFULL + 2;
+    static constexpr int B_S1FULL = B_QEMPTY + QST;   // S1^T (and S2^T issued behind it) in flight
+    static constexpr int B_S1FREE = B_S1FULL + 1;     // the dS warps hold S1^T in registers
+    static constexpr int B_DPFULL = B_S1FREE + 1;     // S2^T and dP^T complete
+    static constexpr int NCH = 4;                    // 16-query chunks per half of the tile
+    static constexpr int B_PFULL = B_DPFULL + 1;      // [chunk]: bf16 operands of one chunk of both halves
+    static constexpr int B_DONE = B_PFULL + NCH;
     static constexpr int NBAR = B_DONE + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
     static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
     // +1024 for aligning the dynamic base; at least 120 KB so that a single
     // CTA (which takes all 512 TMEM columns) is resident per SM.
     static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u) ? USED + 1024 : 120u * 1024u;
-    // Tensor memory: for each half of the query tile (32 queries), S1^T,
-    // S2^T, dP^T (32 columns each; dS1^T, dS2^T and (A1 - lambda A2)^T in
-    // bf16 are written over their first 16), then the dV, dK1, dK2
-    // accumulators.
-    static constexpr int HQ = BQ / 2;                  // queries per half
-    static constexpr uint32_t TM_HALF = 96, TM_S1 = 0, TM_S2 = 32, TM_DP = 64;
-    static constexpr uint32_t TM_DV = 256, TM_DK1 = 256 + DV, TM_DK2 = 256 + DV + D;
+    // Tensor memory: the dV, dK1, dK2 accumulators (dv + 2d columns), then
+    // two 128-column score regions.  Region A holds S1^T, then dP^T, then the
+    // bf16 dS1^T and dS2^T; region B holds S2^T, then the bf16
+    // (A1 - lambda A2)^T.  In bf16 the 16 queries of k-step k (queries
+    // [16 k, 16 k + 16)) pack into 8 columns: dS1^T at A + 16 k, dS2^T at
+    // A + 16 k + 8, (A1 - lambda A2)^T at B + 16 k, inside the columns their
+    // own fp32 values came from.
+    static constexpr uint32_t TM_DV = 0, TM_DK1 = DV, TM_DK2 = DV + D, TM_A = 256, TM_B = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 320;
     // Q/K rows are one swizzle span wide (128 or 64 bytes); dO and V come in
@@ -571,10 +581,18 @@ struct BwdDkvLayout {
     static constexpr uint32_t QK_SWZ = QK_ROW == 128 ? SWZ_128B : SWZ_64B;
     static constexpr uint32_t QK_SBO = 8 * QK_ROW;
     static_assert((D == 64 && DV == 128) || (D == 32 && DV == 64), "backward widths");
-    static_assert(STAGE % 1024 == 0 && RC_BYTES <= 1024, "stage layout");
+    static_assert(STAGE % 1024 == 0, "stage layout");
+    static_assert(DV + 2 * D <= TM_A, "accumulators below the score regions");
     static_assert(SMEM_BYTES <= 227u * 1024u && SMEM_BYTES > 114u * 1024u, "one CTA per SM");
 };
 
+// One CTA owns 128 keys and walks the 128-query tiles that see them.  Per
+// tile the tensor core computes S1^T = K1 Q1^T and S2^T = K2 Q2^T (M = 128
+// keys, N = 128 queries), then dP^T = V dO^T into S1^T's columns once the dS
+// warps hold S1^T; the dS warps (two per TMEM lane quarter, 64 queries each)
+// form A1^T, then A2^T, dS1^T, dS2^T and (A1 - lambda A2)^T in two 32-query
+// chunks, and the gradient products dV += (A1 - lambda A2)^T dO,
+// dK_r += dS_r^T Q_r of the first chunk run while the second is computed.
 template <int D, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
 bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
@@ -605,10 +623,10 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             mbar_init(bar(L::B_QFULL + s), 1);
             mbar_init(bar(L::B_QEMPTY + s), 1);
         }
-        for (int hh = 0; hh < 2; ++hh) {
-            mbar_init(bar(L::B_SFULL + hh), 1);
-            mbar_init(bar(L::B_PFULL + hh), 4);
-        }
+        mbar_init(bar(L::B_S1FULL), 1);
+        mbar_init(bar(L::B_S1FREE), 8);
+        mbar_init(bar(L::B_DPFULL), 1);
+        for (int c = 0; c < L::NCH; ++c) mbar_init(bar(L::B_PFULL + c), 8);
         mbar_init(bar(L::B_DONE), 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_q1);
@@ -651,7 +669,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 for (int c = 0; c < DV / 64; ++c)
                     tma_load_4d(st + L::ST_DO + (uint32_t)c * L::DO_BOX, &tm_do, bar(L::B_QFULL + qs), c * 64, i0, h,
                                 b);
-                bulk_load(st + L::ST_RC, p.rowc + bh * p.Nq_pad + i0, L::RC_BYTES, bar(L::B_QFULL + qs));
+                bulk_load(st + L::ST_RC, p.rowt + (bh * p.Nq_pad + i0) * 4, L::RC_BYTES, bar(L::B_QFULL + qs));
                 ++issued;
             }
             mbar_wait(bar(L::B_KV), 0, ERR_SITE_BWD_DRAIN);
@@ -664,7 +682,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(L::BK, L::HQ, false);   // S^T, dP^T of one half
+            constexpr uint32_t idesc_s = idesc_bf16_f32(L::BK, L::BQ, false);   // S^T, dP^T
             constexpr uint32_t idesc_dv = idesc_bf16_f32(L::BK, DV, true);      // dV: dO MN-major
             constexpr uint32_t idesc_dk = idesc_bf16_f32(L::BK, D, true);       // dK: Q MN-major
             bool ok = mbar_wait(bar(L::B_KV), 0, ERR_SITE_BWD_MMA);
@@ -677,78 +695,73 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             const uint64_t ddo0 = smem_desc(sb + L::OFF_Q + L::ST_DO, 16, 1024, SWZ_128B);     // dO (K-major)
             const uint64_t ddom0 = smem_desc(sb + L::OFF_Q + L::ST_DO, L::DO_BOX, 1024, SWZ_128B);   // dO MN-major
             constexpr uint64_t STAGE16 = L::STAGE >> 4, Q2OFF = L::ST_Q2 >> 4;
-            // 32 rows of the Q tiles and of the (128-byte-row) dO boxes
-            constexpr uint64_t QHALF16 = (L::HQ * L::QK_ROW) >> 4, DOHALF16 = (L::HQ * 128) >> 4;
-            // The two halves of each query tile alternate: while the dS warps
-            // of one half work, the tensor core runs the other half's
-            // gradients and next scores.
-            for (int t = 0; t <= n_t && ok; ++t) {
+            const uint32_t ta = tmem + L::TM_A, tb = tmem + L::TM_B;
+            for (int t = 0; t < n_t && ok; ++t) {
                 const int qs = t % L::QST;
-                if (t < n_t) {
-                    ok = mbar_wait(bar(L::B_QFULL + qs), (t / L::QST) & 1, ERR_SITE_BWD_MMA);
+                const uint64_t st = (uint64_t)qs * STAGE16;
+                ok = mbar_wait(bar(L::B_QFULL + qs), (t / L::QST) & 1, ERR_SITE_BWD_MMA);
+                if (!ok) break;
+                tc_fence_after();
+                // S1^T into region A, S2^T into region B: the MMA pipe runs in
+                // issue order, so these follow the previous tile's gradient
+                // products that read both regions.
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                    mma_ss(ta, dk1 + (uint64_t)(2 * k), dq0 + st + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
+                mma_commit(bar(L::B_S1FULL));
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k)
+                    mma_ss(tb, dk2 + (uint64_t)(2 * k), dq0 + st + Q2OFF + (uint64_t)(2 * k), idesc_s,
+                           k > 0 ? 1u : 0u);
+                // dP^T = V dO^T over S1^T once the dS warps hold it: k over
+                // dv, two 64-column boxes of each operand.
+                ok = mbar_wait(bar(L::B_S1FREE), t & 1, ERR_SITE_BWD_MMA);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < DV / 16; ++k)
+                    mma_ss(ta, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
+                           ddo0 + st + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
+                           k > 0 ? 1u : 0u);
+                mma_commit(bar(L::B_DPFULL));
+                // Gradients, chunk by chunk: chunk c is k-step c of the
+                // first half and k-step 4 + c of the second.
+#pragma unroll
+                for (int c = 0; c < L::NCH; ++c) {
+                    ok = mbar_wait(bar(L::B_PFULL + c), t & 1, ERR_SITE_BWD_MMA);
                     if (!ok) break;
                     tc_fence_after();
-                }
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const uint32_t th = tmem + (uint32_t)hh * L::TM_HALF;
-                    if (t >= 1) {
-                        // Gradients of the previous tile's half hh: A operands
-                        // are the bf16 tiles the dS warps wrote over its scores.
-                        const int tp = t - 1;
-                        const uint64_t st = (uint64_t)(tp % L::QST) * STAGE16;
-                        const uint64_t sq = st + (uint64_t)hh * QHALF16, sd = st + (uint64_t)hh * DOHALF16;
-                        ok = mbar_wait(bar(L::B_PFULL + hh), tp & 1, ERR_SITE_BWD_MMA);
-                        if (!ok) break;
-                        tc_fence_after();
-#pragma unroll
-                        for (int k = 0; k < L::HQ / 16; ++k) {
-                            const uint64_t kd = (uint64_t)(k * (16 * 128 >> 4)), kq = (uint64_t)(k * (16 * L::QK_ROW >> 4));
-                            const uint32_t acc = (tp > 0 || hh > 0 || k > 0) ? 1u : 0u;
-                            mma_ts(tmem + L::TM_DV, th + L::TM_DP + 8u * k, ddom0 + sd + kd, idesc_dv, acc);
-                            mma_ts(tmem + L::TM_DK1, th + L::TM_S1 + 8u * k, dqm0 + sq + kq, idesc_dk, acc);
-                            mma_ts(tmem + L::TM_DK2, th + L::TM_S2 + 8u * k, dqm0 + sq + Q2OFF + kq, idesc_dk, acc);
-                        }
-                        if (hh == 1) mma_commit(bar(L::B_QEMPTY + tp % L::QST));
-                    }
-                    if (t < n_t) {
-                        const uint64_t st = (uint64_t)qs * STAGE16;
-                        const uint64_t sq = st + (uint64_t)hh * QHALF16, sd = st + (uint64_t)hh * DOHALF16;
-                        // dP^T = V dO^T: k over dv, two 64-column boxes of each operand.
-#pragma unroll
-                        for (int k = 0; k < DV / 16; ++k)
-                            mma_ss(th + L::TM_DP, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
-                                   ddo0 + sd + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
-                                   k > 0 ? 1u : 0u);
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k)
-                            mma_ss(th + L::TM_S1, dk1 + (uint64_t)(2 * k), dq0 + sq + (uint64_t)(2 * k), idesc_s,
-                                   k > 0 ? 1u : 0u);
-#pragma unroll
-                        for (int k = 0; k < D / 16; ++k)
-                            mma_ss(th + L::TM_S2, dk2 + (uint64_t)(2 * k), dq0 + sq + Q2OFF + (uint64_t)(2 * k),
-                                   idesc_s, k > 0 ? 1u : 0u);
-                        mma_commit(bar(L::B_SFULL + hh));
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int k = L::NCH * hh + c;   // queries [16 k, 16 k + 16) of the tile
+                        const uint64_t kd = (uint64_t)(k * (16 * 128 >> 4)), kq = (uint64_t)(k * (16 * L::QK_ROW >> 4));
+                        const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+                        const uint32_t col = 16u * k;
+                        mma_ts(tmem + L::TM_DV, tb + col, ddom0 + st + kd, idesc_dv, acc);
+                        mma_ts(tmem + L::TM_DK1, ta + col, dqm0 + st + kq, idesc_dk, acc);
+                        mma_ts(tmem + L::TM_DK2, ta + col + 8u, dqm0 + st + Q2OFF + kq, idesc_dk, acc);
                     }
                 }
+                if (!ok) break;
+                mma_commit(bar(L::B_QEMPTY + qs));
             }
             mma_commit(bar(L::B_DONE));
         }
         __syncwarp();
     } else {
         // ------------------------------------------------------------ dS (warps 2-9)
-        const int hf = (warp - 2) >> 2;         // half: query columns [32 hf, 32 hf + 32) of each tile
+        const int hf = (warp - 2) >> 2;         // half: query columns [64 hf, 64 hf + 64) of each tile
         const int wq = warp & 3;                // TMEM lane quarter
         const int row = wq * 32 + lane;         // key row within the tile
         const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
-        const uint32_t th = tmem + t_lane + (uint32_t)hf * L::TM_HALF;
+        const uint32_t ta = tmem + t_lane + L::TM_A + 64u * hf, tb = tmem + t_lane + L::TM_B + 64u * hf;
         const int kj = k0 + row;
         const float sl2 = p.scale_log2;
-        const float lam = p.lambda;
+        const float nlam = -p.lambda;
         bool ok = true;
         for (int t = 0; t < n_t; ++t) {
             const int qs = t % L::QST;
-            ok = mbar_wait(bar(L::B_SFULL + hf), t & 1, ERR_SITE_BWD_SOFTMAX);
+            ok = mbar_wait(bar(L::B_S1FULL), t & 1, ERR_SITE_BWD_SOFTMAX);
             // The row constants came in with this stage's copies: observe that
             // barrier too (its phase cannot move on before this tile's PFULL
             // arrivals).
@@ -756,39 +769,94 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            uint32_t s1[32], s2[32], dp[32];
-            tmem_ld32(th + L::TM_S1, s1);
-            tmem_ld32(th + L::TM_S2, s2);
-            tmem_ld32(th + L::TM_DP, dp);
-            const float4* rcs = reinterpret_cast<const float4*>(smem + L::OFF_Q + (uint32_t)qs * L::STAGE + L::ST_RC) +
-                                L::HQ * hf;
-            const int qbase = (t0 + t) * L::BQ + L::HQ * hf;   // query of column 0
-            // Causal: key kj is hidden from query q iff kj > q + diag.
-            const bool masked = CAUSAL && (kj > qbase + diag);
-            uint32_t w1[16], w2[16], wd[16];
+            // Row constants of this half's 64 queries, negated: -lse1 log2 e,
+            // -lse2 log2 e, -D1, -D2 at rows 0, 128, 256, 384.
+            const float* rct =
+                reinterpret_cast<const float*>(smem + L::OFF_Q + (uint32_t)qs * L::STAGE + L::ST_RC) + 64 * hf;
+            const int qbase = (t0 + t) * L::BQ + 64 * hf;   // query of column 0
+            // Causal: key kj is hidden from query qbase + i iff i < lim.  The
+            // test runs only in warps that hold a hidden pair (warp-uniform).
+            const int lim = kj - qbase - diag;
+            const bool wmask = CAUSAL && (k0 + 32 * wq + 31 - qbase - diag > 0);
+            float p1[64];
+            {
+                uint32_t s1[64];
+                tmem_ld64(ta, s1);
+                // S1^T is in registers: its columns may take dP^T.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::B_S1FREE));
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float4 ra = rcs[i], rb = rcs[i + 1];
-                float p10 = fast_exp2(fmaf(__uint_as_float(s1[i]), sl2, -ra.x));
-                float p11 = fast_exp2(fmaf(__uint_as_float(s1[i + 1]), sl2, -rb.x));
-                float p20 = fast_exp2(fmaf(__uint_as_float(s2[i]), sl2, -ra.y));
-                float p21 = fast_exp2(fmaf(__uint_as_float(s2[i + 1]), sl2, -rb.y));
-                if (masked) {
-                    if (kj > qbase + i + diag) p10 = p20 = 0.0f;
-                    if (kj > qbase + i + 1 + diag) p11 = p21 = 0.0f;
+                for (int j = 0; j < 64; j += 4) {
+                    const float4 l = *reinterpret_cast<const float4*>(rct + j);
+                    float x0, x1, x2, x3;
+                    fma2(x0, x1, __uint_as_float(s1[j]), __uint_as_float(s1[j + 1]), sl2, sl2, l.x, l.y);
+                    fma2(x2, x3, __uint_as_float(s1[j + 2]), __uint_as_float(s1[j + 3]), sl2, sl2, l.z, l.w);
+                    p1[j] = fast_exp2(x0);
+                    p1[j + 1] = fast_exp2(x1);
+                    p1[j + 2] = fast_exp2(x2);
+                    p1[j + 3] = fast_exp2(x3);
                 }
-                const float d0 = __uint_as_float(dp[i]), d1 = __uint_as_float(dp[i + 1]);
-                w1[i >> 1] = pack_bf16x2(p10 * (d0 - ra.z), p11 * (d1 - rb.z));
-                w2[i >> 1] = pack_bf16x2(-lam * p20 * (d0 - ra.w), -lam * p21 * (d1 - rb.w));
-                wd[i >> 1] = pack_bf16x2(p10 - lam * p20, p11 - lam * p21);
+                if (wmask) {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) p1[j] = j < lim ? 0.0f : p1[j];
+                }
             }
-            tmem_st16(th + L::TM_S1, w1);
-            tmem_st16(th + L::TM_S2, w2);
-            tmem_st16(th + L::TM_DP, wd);
-            tmem_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::B_PFULL + hf));
+            ok = mbar_wait(bar(L::B_DPFULL), t & 1, ERR_SITE_BWD_SOFTMAX);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            // Four 16-query chunks; the gradient products of chunk c start
+            // while chunk c + 1 is computed.
+#pragma unroll
+            for (int c = 0; c < L::NCH; ++c) {
+                uint32_t s2[16], dp[16];
+                tmem_ld16x2(tb + 16u * c, s2, ta + 16u * c, dp);
+                float e[16];
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    const float4 l = *reinterpret_cast<const float4*>(rct + 128 + 16 * c + j);
+                    float x0, x1, x2, x3;
+                    fma2(x0, x1, __uint_as_float(s2[j]), __uint_as_float(s2[j + 1]), sl2, sl2, l.x, l.y);
+                    fma2(x2, x3, __uint_as_float(s2[j + 2]), __uint_as_float(s2[j + 3]), sl2, sl2, l.z, l.w);
+                    e[j] = fast_exp2(x0);
+                    e[j + 1] = fast_exp2(x1);
+                    e[j + 2] = fast_exp2(x2);
+                    e[j + 3] = fast_exp2(x3);
+                }
+                if (wmask) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) e[j] = 16 * c + j < lim ? 0.0f : e[j];
+                }
+                uint32_t w1[8], w2[8], wd[8];
+#pragma unroll
+                for (int j = 0; j < 16; j += 4) {
+                    const float4 n1 = *reinterpret_cast<const float4*>(rct + 256 + 16 * c + j);
+                    const float4 n2 = *reinterpret_cast<const float4*>(rct + 384 + 16 * c + j);
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; h2 += 2) {
+                        const int q = 16 * c + j + h2;   // column within the half
+                        const float d0 = __uint_as_float(dp[j + h2]), d1 = __uint_as_float(dp[j + h2 + 1]);
+                        float u0, u1, v0, v1, g0, g1, a0, a1, b0, b1, c0, c1;
+                        add2(u0, u1, d0, d1, h2 ? n1.z : n1.x, h2 ? n1.w : n1.y);   // dP - D1
+                        add2(v0, v1, d0, d1, h2 ? n2.z : n2.x, h2 ? n2.w : n2.y);   // dP - D2
+                        mul2(g0, g1, e[j + h2], e[j + h2 + 1], nlam, nlam);        // -lambda A2
+                        mul2(a0, a1, p1[q], p1[q + 1], u0, u1);                    // dS1
+                        mul2(b0, b1, g0, g1, v0, v1);                              // dS2
+                        add2(c0, c1, p1[q], p1[q + 1], g0, g1);                    // A1 - lambda A2
+                        w1[(j + h2) >> 1] = pack_bf16x2(a0, a1);
+                        w2[(j + h2) >> 1] = pack_bf16x2(b0, b1);
+                        wd[(j + h2) >> 1] = pack_bf16x2(c0, c1);
+                    }
+                }
+                tmem_st8(ta + 16u * c, w1);
+                tmem_st8(ta + 16u * c + 8u, w2);
+                tmem_st8(tb + 16u * c, wd);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::B_PFULL + c));
+            }
         }
         // ------------------------------------------------------------ epilogue
         mbar_wait(bar(L::B_DONE), 0, ERR_SITE_BWD_EPILOGUE);

@@ -151,7 +151,8 @@ BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int dv) {
     w.nchunk = w.Nq_pad / kBwdPrepRows;
     w.off_do = 0;
     w.off_rowc = align256(BH * Nq * dv * 2);
-    w.off_gpart = w.off_rowc + align256(BH * w.Nq_pad * 16);
+    w.off_rowt = w.off_rowc + align256(BH * w.Nq_pad * 16);
+    w.off_gpart = w.off_rowt + align256(BH * w.Nq_pad * 16);
     w.off_lpart = w.off_gpart + align256(BH * w.nchunk * dv * 4);
     w.total = w.off_lpart + align256(BH * w.nchunk * 4);
     return w;
@@ -182,6 +183,7 @@ static int launch_backward_t(const BwdArgs& a, cudaStream_t st) {
     p.lse = a.lse;
     p.dout = reinterpret_cast<uint16_t*>(ws + w.off_do);
     p.rowc = reinterpret_cast<float4*>(ws + w.off_rowc);
+    p.rowt = reinterpret_cast<float*>(ws + w.off_rowt);
     p.gpart = reinterpret_cast<float*>(ws + w.off_gpart);
     p.lpart = reinterpret_cast<float*>(ws + w.off_lpart);
     p.dq1 = static_cast<uint16_t*>(a.dq1);

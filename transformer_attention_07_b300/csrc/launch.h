@@ -78,7 +78,7 @@ struct BwdArgs {
 // Workspace of the backward pass: do (bf16), the per-row constants, and the
 // dgamma / dlambda partial sums, each 256-byte aligned.
 struct BwdWorkspace {
-    size_t off_do, off_rowc, off_gpart, off_lpart, total;
+    size_t off_do, off_rowc, off_rowt, off_gpart, off_lpart, total;
     int Nq_pad, nchunk;
 };
 BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int dv);

@@ -242,23 +242,29 @@ template <int D, int DV>
 struct BwdDqLayout {
     static constexpr int BM = 128;   // query rows per CTA (MMA M)
     static constexpr int BN = 128;   // keys per tile (MMA N of S and dP)
-    static constexpr int KST = 2;    // K1/K2/V ring depth
+    // K1/K2 and V come in separate rings: V is read by the first product of
+    // a tile (dP, issued a tile ahead), K by the last (dQ), so V runs deeper.
+    static constexpr int KST = 2;    // K1/K2 ring depth
+    static constexpr int VST = 3;    // V ring depth
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t DO_BOX = BM * 128;       // one 64-column box of dO
     static constexpr uint32_t DO_BYTES = BM * DV * 2;
     static constexpr uint32_t K_BYTES = BN * D * 2;
     static constexpr uint32_t V_BOX = BN * 128;
     static constexpr uint32_t V_BYTES = BN * DV * 2;
-    static constexpr uint32_t STAGE = 2 * K_BYTES + V_BYTES;   // K1, K2, V
+    static constexpr uint32_t KSTAGE = 2 * K_BYTES;   // K1, K2
     static constexpr uint32_t OFF_Q1 = 0;
     static constexpr uint32_t OFF_Q2 = Q_BYTES;
     static constexpr uint32_t OFF_DO = 2 * Q_BYTES;
     static constexpr uint32_t OFF_K = OFF_DO + DO_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_K + KST * STAGE;
+    static constexpr uint32_t OFF_V = OFF_K + KST * KSTAGE;
+    static constexpr uint32_t OFF_BAR = OFF_V + VST * V_BYTES;
     static constexpr int B_Q = 0;
     static constexpr int B_KFULL = 1;
     static constexpr int B_KEMPTY = B_KFULL + KST;
-    static constexpr int B_SFULL = B_KEMPTY + KST;   // [map]: S_r (and dP) of the tile in TMEM
+    static constexpr int B_VFULL = B_KEMPTY + KST;
+    static constexpr int B_VEMPTY = B_VFULL + VST;
+    static constexpr int B_SFULL = B_VEMPTY + VST;   // [map]: S_r (and dP) of the tile in TMEM
     static constexpr int B_DPFREE = B_SFULL + 2;     // both maps have dP in registers
     static constexpr int B_PFULL = B_DPFREE + 1;     // [map]: dS_r written over S_r
     static constexpr int B_DQFULL = B_PFULL + 2;
@@ -312,6 +318,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             mbar_init(bar(L::B_KFULL + s), 1);
             mbar_init(bar(L::B_KEMPTY + s), 1);
         }
+        for (int s = 0; s < L::VST; ++s) {
+            mbar_init(bar(L::B_VFULL + s), 1);
+            mbar_init(bar(L::B_VEMPTY + s), 1);
+        }
         for (int r = 0; r < 2; ++r) {
             mbar_init(bar(L::B_SFULL + r), 1);
             mbar_init(bar(L::B_PFULL + r), 4);
@@ -345,25 +355,42 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 #pragma unroll
             for (int c = 0; c < DV / 64; ++c)
                 tma_load_4d(sb + L::OFF_DO + (uint32_t)c * L::DO_BOX, &tm_do, bar(L::B_Q), c * 64, q0, h, b);
-            int issued = 0;
+            // V tile j goes VST - 1 tiles ahead of K tile j.
+            auto load_v = [&](int j) -> bool {
+                const int vs = j % L::VST;
+                if (!mbar_wait(bar(L::B_VEMPTY + vs), ((j / L::VST) & 1) ^ 1, ERR_SITE_BWD_PRODUCER)) return false;
+                const uint32_t st = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
+                mbar_arrive_expect_tx(bar(L::B_VFULL + vs), L::V_BYTES);
+#pragma unroll
+                for (int c = 0; c < DV / 64; ++c)
+                    tma_load_4d(st + (uint32_t)c * L::V_BOX, &tm_v, bar(L::B_VFULL + vs), c * 64, j * L::BN, h, b);
+                return true;
+            };
+            int issued_k = 0, issued_v = 0;
+            for (int j = 0; j < L::VST - 1 && j < n_kv && ok; ++j) ok = load_v(j), issued_v += ok;
             for (int j = 0; j < n_kv && ok; ++j) {
                 const int ks = j % L::KST;
                 ok = mbar_wait(bar(L::B_KEMPTY + ks), ((j / L::KST) & 1) ^ 1, ERR_SITE_BWD_PRODUCER);
                 if (!ok) break;
-                const uint32_t st = sb + L::OFF_K + (uint32_t)ks * L::STAGE;
-                mbar_arrive_expect_tx(bar(L::B_KFULL + ks), L::STAGE);
+                const uint32_t st = sb + L::OFF_K + (uint32_t)ks * L::KSTAGE;
+                mbar_arrive_expect_tx(bar(L::B_KFULL + ks), L::KSTAGE);
                 tma_load_4d(st, &tm_k1, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
                 tma_load_4d(st + L::K_BYTES, &tm_k2, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
-#pragma unroll
-                for (int c = 0; c < DV / 64; ++c)
-                    tma_load_4d(st + 2 * L::K_BYTES + (uint32_t)c * L::V_BOX, &tm_v, bar(L::B_KFULL + ks), c * 64,
-                                j * L::BN, h, b);
-                ++issued;
+                ++issued_k;
+                if (j + L::VST - 1 < n_kv) {
+                    ok = load_v(j + L::VST - 1);
+                    issued_v += ok;
+                }
             }
+            // Every copy lands before the CTA exits.
             mbar_wait(bar(L::B_Q), 0, ERR_SITE_BWD_DRAIN);
-            for (int s = 0; s < L::KST && s < issued; ++s) {
-                const int last = s + ((issued - 1 - s) / L::KST) * L::KST;
+            for (int s = 0; s < L::KST && s < issued_k; ++s) {
+                const int last = s + ((issued_k - 1 - s) / L::KST) * L::KST;
                 mbar_wait(bar(L::B_KFULL + s), (last / L::KST) & 1, ERR_SITE_BWD_DRAIN);
+            }
+            for (int s = 0; s < L::VST && s < issued_v; ++s) {
+                const int last = s + ((issued_v - 1 - s) / L::VST) * L::VST;
+                mbar_wait(bar(L::B_VFULL + s), (last / L::VST) & 1, ERR_SITE_BWD_DRAIN);
             }
         }
         __syncwarp();
@@ -379,8 +406,8 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             const uint64_t ddo = smem_desc(sb + L::OFF_DO, 16, 1024, SWZ_128B);
             const uint64_t dk0 = smem_desc(sb + L::OFF_K, 16, L::QK_SBO, L::QK_SWZ);                 // K1, stage 0
             const uint64_t dkm0 = smem_desc(sb + L::OFF_K, L::K_BYTES, L::QK_SBO, L::QK_SWZ);        // K1 as MN-major B
-            const uint64_t dv0 = smem_desc(sb + L::OFF_K + 2 * L::K_BYTES, 16, 1024, SWZ_128B);  // V, stage 0
-            constexpr uint64_t STAGE16 = L::STAGE >> 4, K2OFF = L::K_BYTES >> 4;
+            const uint64_t dv0 = smem_desc(sb + L::OFF_V, 16, 1024, SWZ_128B);                       // V, stage 0
+            constexpr uint64_t KSTAGE16 = L::KSTAGE >> 4, VSTAGE16 = L::V_BYTES >> 4, K2OFF = L::K_BYTES >> 4;
             // dP = dO V^T: k over dv, two 64-column boxes of each operand.
             auto dp_mma = [&](uint64_t so) {
 #pragma unroll
@@ -405,38 +432,52 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
                            dkm0 + so + (r ? K2OFF : 0) + (uint64_t)(k * (16 * L::QK_ROW >> 4)), idesc_dq,
                            (!first || k > 0) ? 1u : 0u);
             };
+            if (ok) ok = mbar_wait(bar(L::B_VFULL + 0), 0, ERR_SITE_BWD_MMA);
             if (ok) ok = mbar_wait(bar(L::B_KFULL + 0), 0, ERR_SITE_BWD_MMA);
             if (ok) {
                 tc_fence_after();
                 dp_mma(0);
+                mma_commit(bar(L::B_VEMPTY + 0));
                 s_mma(0, 0);
                 mma_commit(bar(L::B_SFULL + 0));
                 s_mma(1, 0);
                 mma_commit(bar(L::B_SFULL + 1));
             }
+            // Per tile j: map 1's dQ product, its next scores, then the next
+            // dP (once both maps hold this tile's dP), which completes the
+            // next tile's inputs for map 1; then map 2's dQ product and next
+            // scores.  Map 2's dS warps load dP last, so the next dP waits for
+            // them only after map 1's products are queued.
             for (int j = 0; j < n_kv && ok; ++j) {
-                const uint64_t so = (uint64_t)(j % L::KST) * STAGE16;
+                const uint64_t so = (uint64_t)(j % L::KST) * KSTAGE16;
                 const bool more = j + 1 < n_kv;
-                const uint64_t sn = (uint64_t)((j + 1) % L::KST) * STAGE16;
+                const uint64_t sn = (uint64_t)((j + 1) % L::KST) * KSTAGE16;
+                ok = mbar_wait(bar(L::B_PFULL + 0), j & 1, ERR_SITE_BWD_MMA);
+                if (!ok) break;
+                tc_fence_after();
+                dq_mma(0, so, j == 0);
                 if (more) {
-                    // dP of the next tile once both maps hold this tile's dP.
                     ok = mbar_wait(bar(L::B_KFULL + (j + 1) % L::KST), ((j + 1) / L::KST) & 1, ERR_SITE_BWD_MMA);
+                    if (!ok) break;
+                    tc_fence_after();
+                    s_mma(0, sn);
+                    const int vs = (j + 1) % L::VST;
+                    ok = mbar_wait(bar(L::B_VFULL + vs), ((j + 1) / L::VST) & 1, ERR_SITE_BWD_MMA);
                     ok = ok && mbar_wait(bar(L::B_DPFREE), j & 1, ERR_SITE_BWD_MMA);
                     if (!ok) break;
                     tc_fence_after();
-                    dp_mma(sn);
+                    dp_mma((uint64_t)vs * VSTAGE16);
+                    mma_commit(bar(L::B_VEMPTY + vs));
+                    mma_commit(bar(L::B_SFULL + 0));
                 }
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    ok = mbar_wait(bar(L::B_PFULL + r), j & 1, ERR_SITE_BWD_MMA);
-                    if (!ok) break;
-                    tc_fence_after();
-                    dq_mma(r, so, j == 0);
-                    if (r == 1) mma_commit(bar(L::B_KEMPTY + j % L::KST));
-                    if (more) {
-                        s_mma(r, sn);
-                        mma_commit(bar(L::B_SFULL + r));
-                    }
+                ok = mbar_wait(bar(L::B_PFULL + 1), j & 1, ERR_SITE_BWD_MMA);
+                if (!ok) break;
+                tc_fence_after();
+                dq_mma(1, so, j == 0);
+                mma_commit(bar(L::B_KEMPTY + j % L::KST));
+                if (more) {
+                    s_mma(1, sn);
+                    mma_commit(bar(L::B_SFULL + 1));
                 }
             }
             mma_commit(bar(L::B_DQFULL));
@@ -454,6 +495,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         const float nlse = -(r ? rc.y : rc.x);
         const float Dr = r ? rc.w : rc.z;
         const float coef = r ? -p.lambda : 1.0f;
+        const float ncd = -coef * Dr;   // dS_r = A_r (coef dP + ncd)
         const float sl2 = p.scale_log2;
         const uint32_t s_col = tmem + t_lane + (r ? L::TM_S2 : L::TM_S1);
         const uint32_t dp_col = tmem + t_lane + L::TM_DP;
@@ -488,8 +530,10 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
                 for (int i = 0; i < 32; i += 2) {
                     float x0, x1;
                     fma2_bcast(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), sl2, nlse);
-                    const float p0 = fast_exp2(x0) * coef, p1 = fast_exp2(x1) * coef;
-                    pk[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dp[i]) - Dr), p1 * (__uint_as_float(dp[i + 1]) - Dr));
+                    float t0, t1, d0, d1;
+                    fma2_bcast(t0, t1, __uint_as_float(dp[i]), __uint_as_float(dp[i + 1]), coef, ncd);
+                    mul2(d0, d1, fast_exp2(x0), fast_exp2(x1), t0, t1);
+                    pk[i >> 1] = pack_bf16x2(d0, d1);
                 }
                 tmem_st16(s_col + 16u * c, pk);
             }

@@ -740,15 +740,15 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             const uint64_t ddom0 = smem_desc(sb + L::OFF_Q + L::ST_DO, L::DO_BOX, 1024, SWZ_128B);   // dO MN-major
             constexpr uint64_t STAGE16 = L::STAGE >> 4, Q2OFF = L::ST_Q2 >> 4;
             const uint32_t ta = tmem + L::TM_A, tb = tmem + L::TM_B;
-            for (int t = 0; t < n_t && ok; ++t) {
-                const int qs = t % L::QST;
-                const uint64_t st = (uint64_t)qs * STAGE16;
-                ok = mbar_wait(bar(L::B_QFULL + qs), (t / L::QST) & 1, ERR_SITE_BWD_MMA);
-                if (!ok) break;
+            // The score products of tile t: S1^T into region A, S2^T into
+            // region B.  They are queued right behind the previous tile's
+            // last gradient products (the MMA pipe runs in issue order, and
+            // those products read both regions), before that tile's stage
+            // is released.
+            auto issue_scores = [&](int t) -> bool {
+                const uint64_t st = (uint64_t)(t % L::QST) * STAGE16;
+                if (!mbar_wait(bar(L::B_QFULL + t % L::QST), (t / L::QST) & 1, ERR_SITE_BWD_MMA)) return false;
                 tc_fence_after();
-                // S1^T into region A, S2^T into region B: the MMA pipe runs in
-                // issue order, so these follow the previous tile's gradient
-                // products that read both regions.
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
                     mma_ss(ta, dk1 + (uint64_t)(2 * k), dq0 + st + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
@@ -757,6 +757,12 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 for (int k = 0; k < D / 16; ++k)
                     mma_ss(tb, dk2 + (uint64_t)(2 * k), dq0 + st + Q2OFF + (uint64_t)(2 * k), idesc_s,
                            k > 0 ? 1u : 0u);
+                return true;
+            };
+            if (ok && n_t > 0) ok = issue_scores(0);
+            for (int t = 0; t < n_t && ok; ++t) {
+                const int qs = t % L::QST;
+                const uint64_t st = (uint64_t)qs * STAGE16;
                 // dP^T = V dO^T over S1^T once the dS warps hold it: k over
                 // dv, two 64-column boxes of each operand.
                 ok = mbar_wait(bar(L::B_S1FREE), t & 1, ERR_SITE_BWD_MMA);
@@ -787,6 +793,10 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                     }
                 }
                 if (!ok) break;
+                if (t + 1 < n_t) {
+                    ok = issue_scores(t + 1);
+                    if (!ok) break;
+                }
                 mma_commit(bar(L::B_QEMPTY + qs));
             }
             mma_commit(bar(L::B_DONE));

@@ -27,9 +27,11 @@
 //                       S_r = Q_r K_r^T, dP = dO V^T on the tensor core,
 //                       dS_r in registers, dQ_r += dS_r K_r (dS_r from TMEM);
 //                       the next tile's scores follow each map's dQ product.
-//   bwd_dkv_kernel      one CTA per 128 keys; walks the query tiles:
+//   bwd_dkv_kernel      one CTA per 128 keys; walks 128-query tiles:
 //                       S_r^T = K_r Q_r^T, dP^T = V dO^T, then
-//                       dV += (A1 - lambda A2)^T dO, dK_r += dS_r^T Q_r.
+//                       dV += (A1 - lambda A2)^T dO, dK_r += dS_r^T Q_r,
+//                       the dS arithmetic in 16-query chunks that overlap
+//                       the previous chunk's products.
 //   bwd_finalize_kernel the dgamma and dlambda sums, in a fixed order.
 // dQ and dK/dV come from separate sweeps (the dQ sweep recomputes S and dP),
 // so every gradient is written once, by one CTA, without atomics: results
@@ -634,9 +636,9 @@ struct BwdDkvLayout {
 // tile the tensor core computes S1^T = K1 Q1^T and S2^T = K2 Q2^T (M = 128
 // keys, N = 128 queries), then dP^T = V dO^T into S1^T's columns once the dS
 // warps hold S1^T; the dS warps (two per TMEM lane quarter, 64 queries each)
-// form A1^T, then A2^T, dS1^T, dS2^T and (A1 - lambda A2)^T in two 32-query
+// form A1^T, then A2^T, dS1^T, dS2^T and (A1 - lambda A2)^T in four 16-query
 // chunks, and the gradient products dV += (A1 - lambda A2)^T dO,
-// dK_r += dS_r^T Q_r of the first chunk run while the second is computed.
+// dK_r += dS_r^T Q_r of chunk c run while chunk c + 1 is computed.
 template <int D, int DV, bool CAUSAL>
 __global__ void __launch_bounds__(320, 1)
 bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,

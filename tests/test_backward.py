@@ -164,3 +164,28 @@ def test_backward_empty_queries_write_zero_key_gradients():
     torch.cuda.synchronize()
     for n in ("dk1", "dk2", "dv", "dlambda", "dgamma"):
         assert grads[n].abs().max().item() == 0.0, n
+
+
+def test_backward_64k_sampled():
+    """The backward configuration bench.py times (causal 64K, B1 H16, the
+    workload's own inputs and dy): dq on sampled rows (the first and last 16
+    and 16 seeded rows), dk and dv on the last 64 keys, which only the last
+    queries see (the oracle visits just those rows)."""
+    from transformer_attention_07_b300.workloads import WORKLOADS, make_dy, make_inputs, sample_rows
+    w = WORKLOADS["long_64k"]
+    inp = make_inputs(w, device="cuda")
+    dy = make_dy(w, device="cuda")
+    q1, k1, q2, k2, v = (inp[n] for n in ("q1", "k1", "q2", "k2", "v"))
+    gamma = inp["gamma"]
+    out, saved = da.fwd_train(q1, k1, q2, k2, v, w.lam, w.lam_init, causal=w.causal, gamma=gamma, eps=w.eps)
+    g = da.bwd(q1, k1, q2, k2, v, dy, saved, w.lam, w.lam_init, causal=w.causal, gamma=gamma, eps=w.eps)
+    torch.cuda.synchronize()
+    assert da.last_device_error() == 0
+    rows = np.asarray(sample_rows(w.Nq, w.seed, n_random=16, edge=16))
+    keys = np.arange(w.Nk - 64, w.Nk)
+    ref = oracle.diffattn_bwd(*cpu(q1, k1, q2, k2, v, dy), w.lam, w.lam_init, causal=w.causal,
+                              gamma=None if gamma is None else gamma.double().cpu(), eps=w.eps, rows=rows, keys=keys)
+    for n in ("dq1", "dq2"):
+        rel_check(n, g[n][:, :, rows].float().cpu().numpy(), ref[n])
+    for n in ("dk1", "dk2", "dv"):
+        rel_check(n, g[n][:, :, keys].float().cpu().numpy(), ref[n])

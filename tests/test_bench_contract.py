@@ -1,0 +1,40 @@
+"""bench.py's contract, checked on the host (no GPU): the reference arm's JSON
+line and the sha-gated traffic table that feeds roofline.traffic."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_reference_arm_prints_one_contract_line():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3", "--ref-rows", "4"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC
+    assert d["unit"] == "TFLOP/s" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3 and d["ms_per_step"] > 0
+    assert d["dtype"] == "f64" and d["data"] == "synthetic" and d["vs_baseline"] is None
+    assert "workload" in d["config"] and "model" not in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_traffic_table_is_used_only_for_the_profiled_source(tmp_path):
+    src = os.path.join(ROOT, "transformer_attention_07_b300", "csrc", "prefill_sm103a.cuh")
+    key = "prefill_kernel<64,128,causal> long_64k"
+    t = bench.traffic_from_profiles(key, src)
+    # The committed table was taken on the committed kernel source.
+    assert isinstance(t, int) and t > 0
+    changed = tmp_path / "prefill_sm103a.cuh"
+    changed.write_bytes(open(src, "rb").read() + b"\n// changed\n")
+    assert bench.traffic_from_profiles(key, str(changed)) is None
+    assert bench.traffic_from_profiles("no such kernel", src) is None

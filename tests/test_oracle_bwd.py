@@ -141,6 +141,25 @@ def test_gradients_vanish_when_lambda_init_is_one():
     assert g["dlambda"] == 0.0
 
 
+def test_single_key_closed_form():
+    """With one key every softmax row is exactly 1, so o = (1 - lambda) v0 for
+    every query: the scores get no gradient (dq = dk = 0 exactly) and
+    dv0 = (1 - lambda) sum_i do_i, where do is the gradient of the GroupNorm
+    output alone (torch autograd through group_norm, a library routine)."""
+    B, H, Nq, d, dv = 1, 2, 5, 4, 8
+    t, dy, gamma = problem(B, H, Nq, 1, d, dv, seed=13)
+    lam, lam_init, eps = 0.35, 0.8, 1e-5
+    g = oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, lam, lam_init, gamma=gamma, eps=eps)
+    for n in ("dq1", "dq2", "dk1", "dk2"):
+        assert np.abs(g[n]).max() == 0.0, n
+    o = torch.tensor(np.broadcast_to((1 - lam) * t["v"], (B, H, Nq, dv)).copy(), requires_grad=True)
+    x = o.permute(0, 2, 1, 3).reshape(B * Nq, H * dv)
+    y = F.group_norm(x, H, weight=torch.tensor(gamma), bias=None, eps=eps) * (1 - lam_init)
+    (y.reshape(B, Nq, H, dv).permute(0, 2, 1, 3) * torch.tensor(dy)).sum().backward()
+    dv_ref = (1 - lam) * o.grad.numpy().sum(axis=2, keepdims=True)
+    assert np.abs(g["dv"] - dv_ref).max() < 1e-12 * max(1.0, np.abs(dv_ref).max())
+
+
 def test_bwd_rejects_bad_arguments():
     t, dy, _ = problem(1, 1, 4, 4, 4, 8, seed=1)
     with pytest.raises(ValueError):

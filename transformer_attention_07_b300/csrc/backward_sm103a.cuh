@@ -602,7 +602,8 @@ struct BwdDkvLayout {
     static constexpr int B_S1FULL = B_QEMPTY + QST;   // S1^T (and S2^T issued behind it) in flight
     static constexpr int B_S1FREE = B_S1FULL + 1;     // the dS warps hold S1^T in registers
     static constexpr int B_DPFULL = B_S1FREE + 1;     // S2^T and dP^T complete
-    static constexpr int NCH = 4;                    // 16-query chunks per half of the tile
+    static constexpr int NCH = 4;                    // chunks per half of the tile
+    static constexpr int CW = 64 / NCH;              // queries per chunk (16 or 32)
     static constexpr int B_PFULL = B_DPFULL + 1;      // [chunk]: bf16 operands of one chunk of both halves
     static constexpr int B_DONE = B_PFULL + NCH;
     static constexpr int NBAR = B_DONE + 1;
@@ -614,10 +615,10 @@ struct BwdDkvLayout {
     // Tensor memory: the dV, dK1, dK2 accumulators (dv + 2d columns), then
     // two 128-column score regions.  Region A holds S1^T, then dP^T, then the
     // bf16 dS1^T and dS2^T; region B holds S2^T, then the bf16
-    // (A1 - lambda A2)^T.  In bf16 the 16 queries of k-step k (queries
-    // [16 k, 16 k + 16)) pack into 8 columns: dS1^T at A + 16 k, dS2^T at
-    // A + 16 k + 8, (A1 - lambda A2)^T at B + 16 k, inside the columns their
-    // own fp32 values came from.
+    // (A1 - lambda A2)^T.  In bf16 each chunk of CW queries packs inside
+    // the columns its own fp32 values came from: dS1^T then dS2^T (CW / 2
+    // columns each) in region A, (A1 - lambda A2)^T in the first CW / 2 of
+    // region B.
     static constexpr uint32_t TM_DV = 0, TM_DK1 = DV, TM_DK2 = DV + D, TM_A = 256, TM_B = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int THREADS = 320;
@@ -776,8 +777,11 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                            ddo0 + st + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
                            k > 0 ? 1u : 0u);
                 mma_commit(bar(L::B_DPFULL));
-                // Gradients, chunk by chunk: chunk c is k-step c of the
-                // first half and k-step 4 + c of the second.
+                // Gradients, chunk by chunk: chunk c is queries
+                // [64 hh + CW c, 64 hh + CW c + CW) of each half hh, CW / 16
+                // k-steps; in bf16 its dS1^T, dS2^T fill the chunk's columns
+                // of region A ([dS1 | dS2], CW / 2 columns each) and
+                // (A1 - lambda A2)^T the first CW / 2 of region B.
 #pragma unroll
                 for (int c = 0; c < L::NCH; ++c) {
                     ok = mbar_wait(bar(L::B_PFULL + c), t & 1, ERR_SITE_BWD_MMA);
@@ -785,13 +789,17 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                     tc_fence_after();
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        const int k = L::NCH * hh + c;   // queries [16 k, 16 k + 16) of the tile
-                        const uint64_t kd = (uint64_t)(k * (16 * 128 >> 4)), kq = (uint64_t)(k * (16 * L::QK_ROW >> 4));
-                        const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-                        const uint32_t col = 16u * k;
-                        mma_ts(tmem + L::TM_DV, tb + col, ddom0 + st + kd, idesc_dv, acc);
-                        mma_ts(tmem + L::TM_DK1, ta + col, dqm0 + st + kq, idesc_dk, acc);
-                        mma_ts(tmem + L::TM_DK2, ta + col + 8u, dqm0 + st + Q2OFF + kq, idesc_dk, acc);
+#pragma unroll
+                        for (int sub = 0; sub < L::CW / 16; ++sub) {
+                            const int k = (64 * hh + L::CW * c) / 16 + sub;   // queries [16 k, 16 k + 16)
+                            const uint64_t kd = (uint64_t)(k * (16 * 128 >> 4)),
+                                           kq = (uint64_t)(k * (16 * L::QK_ROW >> 4));
+                            const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
+                            const uint32_t col = 64u * hh + L::CW * c + 8u * sub;
+                            mma_ts(tmem + L::TM_DV, tb + col, ddom0 + st + kd, idesc_dv, acc);
+                            mma_ts(tmem + L::TM_DK1, ta + col, dqm0 + st + kq, idesc_dk, acc);
+                            mma_ts(tmem + L::TM_DK2, ta + col + L::CW / 2, dqm0 + st + Q2OFF + kq, idesc_dk, acc);
+                        }
                     }
                 }
                 if (!ok) break;
@@ -862,16 +870,20 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            // Four 16-query chunks; the gradient products of chunk c start
+            // NCH chunks of CW queries; the gradient products of chunk c start
             // while chunk c + 1 is computed.
+            constexpr int CW = L::CW;
 #pragma unroll
             for (int c = 0; c < L::NCH; ++c) {
-                uint32_t s2[16], dp[16];
-                tmem_ld16x2(tb + 16u * c, s2, ta + 16u * c, dp);
-                float e[16];
+                uint32_t s2[CW], dp[CW];
+                if constexpr (CW == 16)
+                    tmem_ld16x2(tb + CW * c, s2, ta + CW * c, dp);
+                else
+                    tmem_ld32x2(tb + CW * c, s2, ta + CW * c, dp);
+                float e[CW];
 #pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    const float4 l = *reinterpret_cast<const float4*>(rct + 128 + 16 * c + j);
+                for (int j = 0; j < CW; j += 4) {
+                    const float4 l = *reinterpret_cast<const float4*>(rct + 128 + CW * c + j);
                     float x0, x1, x2, x3;
                     fma2(x0, x1, __uint_as_float(s2[j]), __uint_as_float(s2[j + 1]), sl2, sl2, l.x, l.y);
                     fma2(x2, x3, __uint_as_float(s2[j + 2]), __uint_as_float(s2[j + 3]), sl2, sl2, l.z, l.w);
@@ -882,16 +894,16 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 }
                 if (wmask) {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) e[j] = 16 * c + j < lim ? 0.0f : e[j];
+                    for (int j = 0; j < CW; ++j) e[j] = CW * c + j < lim ? 0.0f : e[j];
                 }
-                uint32_t w1[8], w2[8], wd[8];
+                uint32_t w1[CW / 2], w2[CW / 2], wd[CW / 2];
 #pragma unroll
-                for (int j = 0; j < 16; j += 4) {
-                    const float4 n1 = *reinterpret_cast<const float4*>(rct + 256 + 16 * c + j);
-                    const float4 n2 = *reinterpret_cast<const float4*>(rct + 384 + 16 * c + j);
+                for (int j = 0; j < CW; j += 4) {
+                    const float4 n1 = *reinterpret_cast<const float4*>(rct + 256 + CW * c + j);
+                    const float4 n2 = *reinterpret_cast<const float4*>(rct + 384 + CW * c + j);
 #pragma unroll
                     for (int h2 = 0; h2 < 4; h2 += 2) {
-                        const int q = 16 * c + j + h2;   // column within the half
+                        const int q = CW * c + j + h2;   // column within the half
                         const float d0 = __uint_as_float(dp[j + h2]), d1 = __uint_as_float(dp[j + h2 + 1]);
                         float u0, u1, v0, v1, g0, g1, a0, a1, b0, b1, c0, c1;
                         add2(u0, u1, d0, d1, h2 ? n1.z : n1.x, h2 ? n1.w : n1.y);   // dP - D1
@@ -905,9 +917,15 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                         wd[(j + h2) >> 1] = pack_bf16x2(c0, c1);
                     }
                 }
-                tmem_st8(ta + 16u * c, w1);
-                tmem_st8(ta + 16u * c + 8u, w2);
-                tmem_st8(tb + 16u * c, wd);
+                if constexpr (CW == 16) {
+                    tmem_st8(ta + CW * c, w1);
+                    tmem_st8(ta + CW * c + CW / 2, w2);
+                    tmem_st8(tb + CW * c, wd);
+                } else {
+                    tmem_st16(ta + CW * c, w1);
+                    tmem_st16(ta + CW * c + CW / 2, w2);
+                    tmem_st16(tb + CW * c, wd);
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();

@@ -321,6 +321,19 @@ const char* diffattn_status_string(int status);
  */
 int diffattn_last_device_error(void* stream);
 
+/*
+ * Diagnostic for the failure path above: launches on `stream` a one-warp
+ * kernel whose only thread waits, through the same bounded wait every kernel
+ * uses, for an mbarrier phase that nothing completes.  After the wait limit
+ * (2 s) the kernel records code 0x601 in the device error word and exits;
+ * the CUDA context stays usable.  Returns DIFFATTN_OK when the launch was
+ * accepted (the code is then read with diffattn_last_device_error), or
+ * DIFFATTN_ERR_CUDA.  Nothing else in the library is affected, except that
+ * a wait of another kernel running at the same time returns early once the
+ * word is set.
+ */
+int diffattn_selftest_wait_timeout(void* stream);
+
 #ifdef __cplusplus
 }
 #endif

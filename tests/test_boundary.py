@@ -36,7 +36,7 @@ def test_header_declares_the_entry_points():
         "diffattn_decode_workspace_bytes", "diffattn_decode", "diffattn_decode_partials_bytes",
         "diffattn_decode_partials", "diffattn_decode_merge",
         "diffattn_decode_noalloc", "diffattn_decode_paged", "diffattn_standard_fwd", "diffattn_status_string",
-        "diffattn_last_device_error"])
+        "diffattn_last_device_error", "diffattn_selftest_wait_timeout"])
 
 
 def test_library_exports_every_declared_symbol(lib):

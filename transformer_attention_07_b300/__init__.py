@@ -20,7 +20,8 @@ import os
 __all__ = [
     "fwd", "fwd_host", "fwd_host_workspace_bytes", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes",
     "standard_fwd", "decode", "decode_paged", "decode_workspace_bytes", "decode_partials", "decode_partials_bytes",
-    "decode_merge", "gather_partials", "decode_sharded", "status_string", "last_device_error", "load", "LIB_PATH",
+    "decode_merge", "gather_partials", "decode_sharded", "status_string", "last_device_error",
+    "selftest_wait_timeout", "load", "LIB_PATH",
     "DiffAttnError", "SUPPORTED_WIDTHS",
 ]
 
@@ -90,6 +91,8 @@ def load():
     lib.diffattn_status_string.restype = ctypes.c_char_p
     lib.diffattn_last_device_error.argtypes = [vp]
     lib.diffattn_last_device_error.restype = i32
+    lib.diffattn_selftest_wait_timeout.argtypes = [vp]
+    lib.diffattn_selftest_wait_timeout.restype = i32
     _lib = lib
     return lib
 
@@ -421,3 +424,11 @@ def decode_sharded(q1, k1, q2, k2, v, lam, lam_init, num_splits=8, gamma=None, e
 def last_device_error(stream=None) -> int:
     """Read and clear the device error word (synchronises ``stream``)."""
     return int(load().diffattn_last_device_error(_stream(stream)))
+
+
+def selftest_wait_timeout(stream=None) -> None:
+    """Launch the diagnostic kernel whose bounded wait runs out (about 2 s);
+    afterwards ``last_device_error`` returns 0x601."""
+    rc = load().diffattn_selftest_wait_timeout(_stream(stream))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_selftest_wait_timeout")

@@ -340,6 +340,12 @@ const char* diffattn_status_string(int status) {
     }
 }
 
+int diffattn_selftest_wait_timeout(void* stream) {
+    return diffattn::launch_selftest_wait(static_cast<cudaStream_t>(stream)) == diffattn::LAUNCH_OK
+               ? DIFFATTN_OK
+               : DIFFATTN_ERR_CUDA;
+}
+
 int diffattn_last_device_error(void* stream) {
     int v = 0;
     if (diffattn::read_and_clear_device_error(static_cast<cudaStream_t>(stream), &v) != diffattn::LAUNCH_OK)

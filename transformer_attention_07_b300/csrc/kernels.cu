@@ -393,6 +393,24 @@ int decode_noalloc_scratch(void** ptr, size_t* bytes) {
     return LAUNCH_OK;
 }
 
+// One thread waits, through the library's bounded wait, for a phase of a
+// freshly initialised mbarrier that nothing arrives on: the wait runs out,
+// records its site in the device error word and returns, and the kernel
+// exits normally.
+__global__ void __launch_bounds__(32, 1) selftest_wait_kernel() {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        fence_mbar_init();
+        mbar_wait(smem_addr(&bar), 0, ERR_SITE_SELFTEST);
+    }
+}
+
+int launch_selftest_wait(cudaStream_t st) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>();
+    return cuda_ok(cudaGetLastError(), "self-test: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+}
+
 int read_and_clear_device_error(cudaStream_t st, int* value) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return LAUNCH_ERR_CUDA;
     int v = 0;

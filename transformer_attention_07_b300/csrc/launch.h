@@ -88,6 +88,7 @@ int launch_backward(const BwdArgs& a, cudaStream_t st);
 int launch_standard(const StandardArgs& a, cudaStream_t st);
 int launch_decode(const DecodeArgs& a, cudaStream_t st);
 int read_and_clear_device_error(cudaStream_t st, int* value);
+int launch_selftest_wait(cudaStream_t st);
 
 // Capacity of the library-owned decode scratch (diffattn_decode_noalloc).
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;

@@ -32,6 +32,7 @@ enum : int {
     ERR_SITE_BWD_DRAIN = 0x405,
     ERR_DECODE_BAD_PAGE = 0x301,      // a block-table entry outside [0, num_pages): clamped, not read
     ERR_DECODE_BAD_LENGTH = 0x302,    // a sequence length outside [1, max_pages * page_size): clamped
+    ERR_SITE_SELFTEST = 0x601,        // diffattn_selftest_wait_timeout: the wait that is meant to run out
 };
 
 // Upper bound of any single wait.  A legitimate wait lasts microseconds (one

@@ -136,12 +136,12 @@ def rank_seed(base_seed: int, rank: int) -> int:
     return base_seed + 1000 * rank
 
 
-def oracle_sample(w, inp_cpu, rows):
+def oracle_sample(w, inp_cpu, rows, gamma=None):
     import oracle
     (o, y), dt = oracle.timed_fwd(*inp_cpu, w.lam, w.lam_init, causal=w.causal, eps=w.eps, rows=rows,
-                                  threads=os.cpu_count() or 1)
+                                  gamma=gamma, threads=os.cpu_count() or 1)
     pairs = w.B * w.H * sum(min(w.Nk, r + (w.Nk - w.Nq) + 1) if w.causal else w.Nk for r in rows)
-    return 4 * (w.d + w.dv) * pairs, dt, pairs
+    return 4 * (w.d + w.dv) * pairs, dt, pairs, y
 
 
 def sample_rows_uniform(N, n, seed):
@@ -173,7 +173,7 @@ def run_reference(args, world, rank):
     flops = secs = 0.0
     for step in range(args.warmup + args.steps):
         rows = sample_rows_uniform(w.Nq, args.ref_rows, 7000 + step)
-        f, dt, _ = oracle_sample(w, cpu, rows)
+        f, dt, _, _ = oracle_sample(w, cpu, rows)
         if step >= args.warmup:
             flops += f
             secs += dt
@@ -552,6 +552,19 @@ def run_cuda(args, world, rank, local):
     line["gpu_launches"] = args.steps * ((1 if do_pre else 0) + (2 if do_dec else 0))
     line["clocks"] = clk.summary()
     line["wall_s_timed"] = wall
+    if do_dec and not args.no_cpu_baseline:
+        # The benchmarked decode's output for the first two batch entries
+        # (every head, every key) against the oracle.
+        import oracle
+        nb = min(2, wd.B)
+        c = [din[k][:nb].cpu() for k in names]
+        g = din["gamma"]
+        _, y_ref = oracle.diffattn_fwd(*c, wd.lam, wd.lam_init, causal=False, eps=wd.eps,
+                                       gamma=None if g is None else g.double().cpu().numpy(),
+                                       threads=os.cpu_count() or 1)
+        got = dout[:nb].float().cpu().numpy()
+        line.setdefault("parity", {})["decode"] = {
+            "heads": nb * wd.H, "max_abs_out": float(abs(got - y_ref).max()), "tol_out": 3e-2}
     if args.only == "all" and not args.no_compare:
         line["single_map_baseline"] = compare_single_map(dev)
         del din
@@ -564,11 +577,16 @@ def run_cuda(args, world, rank, local):
     if do_pre and not args.no_cpu_baseline:
         cpu = [pin[k].cpu() for k in names]
         rows = sample_rows_uniform(wp.Nq, args.cpu_rows, 4242)
-        f, dt, _ = oracle_sample(wp, cpu, rows)
+        f, dt, _, y_ref = oracle_sample(wp, cpu, rows,
+                                        None if pin["gamma"] is None else pin["gamma"].double().cpu().numpy())
         line["cpu_baseline"] = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
                                 "kind": "oracle", "seconds": dt,
                                 "sample": f"{len(rows)} seeded query rows x {wp.H} heads of {wp.name} "
                                           "(fp64, every visible key of each row)"}
+        # The same oracle rows against the benchmarked prefill's own output.
+        got = pout[:, :, rows].float().cpu().numpy()
+        line.setdefault("parity", {})["prefill"] = {
+            "rows": len(rows) * wp.B * wp.H, "max_abs_out": float(abs(got - y_ref).max()), "tol_out": 3e-2}
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

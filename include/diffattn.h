@@ -328,9 +328,10 @@ int diffattn_last_device_error(void* stream);
  * (2 s) the kernel records code 0x601 in the device error word and exits;
  * the CUDA context stays usable.  Returns DIFFATTN_OK when the launch was
  * accepted (the code is then read with diffattn_last_device_error), or
- * DIFFATTN_ERR_CUDA.  Nothing else in the library is affected, except that
- * a wait of another kernel running at the same time returns early once the
- * word is set.
+ * DIFFATTN_ERR_CUDA.  While the word is set, every bounded wait of the
+ * library's kernels gives up at its first slow-path check (a failed wait
+ * makes the rest of the grid stop early), so read the word, which clears it,
+ * before launching other work.
  */
 int diffattn_selftest_wait_timeout(void* stream);
 

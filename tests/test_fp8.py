@@ -90,3 +90,26 @@ def test_fp8_long_sampled_rows():
                                        causal=True, rows=rows)
     assert np.abs(pre[:, :, rows].cpu().numpy() - o_ref).max() <= TOL_PRE
     assert np.abs(out[:, :, rows].float().cpu().numpy() - y_ref).max() <= TOL_OUT
+
+
+def test_fp8_benchmarked_configuration_sampled_rows():
+    """The configuration bench.py times for the fp8 row: the long_64k workload
+    (causal, B1 H16 N65536) quantised exactly as the bench does (per-head
+    amax / 448), sampled rows against the oracle on the dequantised values."""
+    from transformer_attention_07_b300.workloads import WORKLOADS, make_inputs, sample_rows
+    w = WORKLOADS["long_64k"]
+    inp = make_inputs(w, device="cuda")
+    qs = [quantise(inp[n].float()) for n in ("q1", "k1", "q2", "k2")]
+    scale = torch.stack([s for _, s, _ in qs]).contiguous().view(-1)
+    pre = torch.empty((w.B, w.H, w.Nq, w.dv), dtype=torch.float32, device="cuda")
+    out = da.fwd_fp8(qs[0][0], qs[1][0], qs[2][0], qs[3][0], inp["v"], scale, w.lam, w.lam_init, causal=w.causal,
+                     gamma=inp["gamma"], eps=w.eps, o_prenorm=pre)
+    torch.cuda.synchronize()
+    assert da.last_device_error() == 0
+    rows = np.asarray(sample_rows(w.Nq, w.seed, n_random=32, edge=16))
+    g = inp["gamma"]
+    o_ref, y_ref = oracle.diffattn_fwd(qs[0][2], qs[1][2], qs[2][2], qs[3][2], inp["v"].cpu().double(), w.lam,
+                                       w.lam_init, causal=w.causal, eps=w.eps,
+                                       gamma=None if g is None else g.double().cpu(), rows=rows)
+    assert np.abs(pre[:, :, rows].cpu().numpy() - o_ref).max() <= TOL_PRE
+    assert np.abs(out[:, :, rows].float().cpu().numpy() - y_ref).max() <= TOL_OUT

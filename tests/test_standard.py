@@ -56,3 +56,21 @@ def test_standard_attention_2k_sampled():
     qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
     o_ref, _ = oracle.diffattn_fwd(qc, kc, qc, kc, vc, 0.0, 0.0, causal=True, rows=rows)
     assert np.abs(out32.cpu().numpy()[:, :, rows] - o_ref).max() <= TOL
+
+
+@pytest.mark.parametrize("shape", [(8, 16, 2048), (4, 16, 4096)])
+def test_standard_attention_benchmarked_configurations(shape):
+    """The single-map baseline exactly as bench.py times it (its own inputs,
+    causal, B8 H16 N2048 and B4 H16 N4096): sampled rows of every head."""
+    from transformer_attention_07_b300.workloads import COMPARE_SHAPES, sample_rows, standard_inputs
+    assert shape in COMPARE_SHAPES
+    B, H, N = shape
+    si = standard_inputs(B, H, N, device="cuda")
+    out32 = torch.empty((B, H, N, 128), dtype=torch.float32, device="cuda")
+    da.standard_fwd(si["q"], si["k"], si["v"], causal=True, out_f32=out32)
+    torch.cuda.synchronize()
+    assert da.last_device_error() == 0
+    rows = sample_rows(N, 2000 + N, n_random=8, edge=4)
+    qc, kc, vc = si["q"].cpu(), si["k"].cpu(), si["v"].cpu()
+    o_ref, _ = oracle.diffattn_fwd(qc, kc, qc, kc, vc, 0.0, 0.0, causal=True, rows=rows)
+    assert np.abs(out32.cpu().numpy()[:, :, rows] - o_ref).max() <= TOL

@@ -57,3 +57,18 @@ def test_host_call_orders_after_earlier_stream_work():
     s.synchronize()
     ref = da.fwd(dev["q1"], dev["k1"], dev["q2"], dev["k2"], dev["v"], 0.6, 0.8, causal=True, gamma=gamma)
     assert torch.equal(out, ref.cpu())
+
+
+def test_host_call_in_the_benchmarked_configuration():
+    """The e2e leg of bench.py: long_64k (causal, B1 H16 N65536) from pinned host
+    buffers with the default chunking equals the device-resident call."""
+    from transformer_attention_07_b300.workloads import WORKLOADS, make_inputs
+    w = WORKLOADS["long_64k"]
+    inp = make_inputs(w, device="cuda")
+    names = ("q1", "k1", "q2", "k2", "v")
+    ref = da.fwd(*(inp[k] for k in names), w.lam, w.lam_init, causal=w.causal, gamma=inp["gamma"], eps=w.eps)
+    host = {k: inp[k].cpu().pin_memory() for k in names}
+    out = da.fwd_host(*(host[k] for k in names), w.lam, w.lam_init, causal=w.causal, gamma=inp["gamma"], eps=w.eps)
+    torch.cuda.current_stream().synchronize()
+    assert da.last_device_error() == 0
+    assert torch.equal(out, ref.cpu())

@@ -74,12 +74,20 @@ class ClockSampler:
         self.proc = None
 
     def __enter__(self):
+        self.first = ""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        if self.proc is not None:
+            # Start timing only once the sampler runs (its start-up takes a
+            # while), so that the samples cover the whole timed region.
+            import select
+            ready, _, _ = select.select([self.proc.stdout], [], [], 5.0)
+            if ready:
+                self.first = self.proc.stdout.readline()
         return self
 
     def __exit__(self, *exc):
@@ -91,6 +99,7 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 self.out, _ = self.proc.communicate()
+        self.out = self.first + (self.out or "")
 
     def summary(self):
         rows = []

@@ -372,6 +372,42 @@ def fp8_throughput(dev, w, inp, reps=10):
             "note": "Q/K e4m3 with per-head scales; QK^T on the 8-bit tensor core, P V in bf16"}
 
 
+def prefill_by_length(dev, reps=5):
+    """The prefill at the other long-context lengths (same token count as the
+    64K workload up to 64K, and the 128K workload at H = 8), each on its own
+    seeded inputs.  Algorithmic TFLOP/s as for the headline number."""
+    import dataclasses
+    import torch
+    import transformer_attention_07_b300 as da
+    from transformer_attention_07_b300.workloads import WORKLOADS, make_inputs
+    stream = torch.cuda.current_stream(dev)
+    base = WORKLOADS["long_64k"]
+    cases = [dataclasses.replace(base, name="long_4k", B=16, Nq=4096, Nk=4096),
+             dataclasses.replace(base, name="long_16k_b4", B=4, Nq=16384, Nk=16384),
+             WORKLOADS["long_128k"]]
+    res = {}
+    for w in cases:
+        inp = make_inputs(w, device=dev)
+        out = torch.empty((w.B, w.H, w.Nq, w.dv), dtype=torch.bfloat16, device=dev)
+        run = lambda: da.fwd(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], w.lam, w.lam_init,
+                             causal=w.causal, gamma=inp["gamma"], eps=w.eps, out=out, stream=stream)
+        for _ in range(3):
+            run()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            run()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if da.last_device_error() != 0:
+            raise RuntimeError(f"device-side error in the prefill at {w.name}")
+        ms = e0.elapsed_time(e1) / reps
+        res[w.name] = {"B": w.B, "H": w.H, "N": w.Nq, "ms": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12}
+        del inp, out
+        torch.cuda.empty_cache()
+    return res
+
+
 def backward_throughput(dev, w, inp, reps=3):
     """Backward pass (prep, dQ sweep, dK/dV sweep, finalize) on workload w,
     after one training forward.  Algorithmic flops per pair 12d + 4dv (S1,
@@ -441,6 +477,9 @@ def run_cuda(args, world, rank, local):
         return 0
     if args.only == "paged":
         print(json.dumps({"decode_paged": paged_decode_throughput(dev, reps=args.steps)}), flush=True)
+        return 0
+    if args.only == "lengths":
+        print(json.dumps({"prefill_by_length": prefill_by_length(dev, reps=args.steps)}), flush=True)
         return 0
     if args.only == "standard":
         print(json.dumps({"single_map_baseline": compare_single_map(dev, reps=args.steps)}), flush=True)
@@ -583,6 +622,7 @@ def run_cuda(args, world, rank, local):
         line["fp8_qk"] = fp8_throughput(dev, wp, pin)
         line["fp8_qk"]["vs_bf16"] = line["prefill_ms"] / line["fp8_qk"]["ms"] - 1.0
         line["decode_small_latency"] = small_decode_latency(dev)
+        line["prefill_by_length"] = prefill_by_length(dev)
     if do_pre and not args.no_cpu_baseline:
         cpu = [pin[k].cpu() for k in names]
         rows = sample_rows_uniform(wp.Nq, args.cpu_rows, 4242)
@@ -615,7 +655,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-compare", action="store_true",
                     help="skip the DiffAttn vs single-map (standard attention) comparison")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward", "fp8", "paged", "standard"],
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "backward", "fp8", "paged", "standard",
+                                       "lengths"],
                     default="all",
                     help="run one stage per step (profiling of a single kernel)")
     ap.add_argument("--prefill-workload", default=PREFILL)

@@ -254,22 +254,12 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             const float m_new = fmaxf(m, fmax3(mx0, mx1, fmaxf(mx2, mx3)) * sl2);
             const bool grow = m_new > m + 8.0f;
-            if (__any_sync(0xffffffffu, grow)) {
-                const float alpha = grow ? fast_exp2(m - m_new) : 1.0f;
-                if (j > 0) {
-#pragma unroll
-                    for (int c = 0; c < L::DV / 32; ++c) {
-                        uint32_t ov[32];
-                        tmem_ld32(tmem + t_lane + o_col + 32u * c, ov);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                        tmem_st32(tmem + t_lane + o_col + 32u * c, ov);
-                    }
-                }
-                if (grow) {
-                    l *= alpha;
-                    m = m_new;
-                }
+            const bool rescale = __any_sync(0xffffffffu, grow) && j > 0;   // warp-uniform
+            float alpha = 1.0f;
+            if (grow) {
+                alpha = fast_exp2(m - m_new);
+                l *= alpha;
+                m = m_new;
             }
             const float nm = (m == -INFINITY) ? 0.f : -m;
             uint32_t pk[64];
@@ -292,6 +282,19 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             l += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
             tmem_st64(tmem + t_lane + s_col, pk);
+            if (rescale) {
+                // O *= alpha once the scores' registers are free; the
+                // previous P V has completed and this tile's waits for the
+                // hand-off below.
+#pragma unroll
+                for (int c = 0; c < L::DV / 32; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tmem + t_lane + o_col + 32u * c, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    tmem_st32(tmem + t_lane + o_col + 32u * c, ov);
+                }
+            }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();

@@ -88,6 +88,28 @@ static bool make_map_bhnd(CUtensorMap* m, const void* base, int B, int H, int N,
 
 // ----------------------------------------------------------------- prefill
 
+// Streaming multiprocessors of the current device (0 if unknown), cached per
+// device.
+static int sm_count() {
+    constexpr int kMaxDevices = 64;
+    static int cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < kMaxDevices) cache[dev] = n;
+    return n;
+}
+
+// Key lengths up to which the prefill runs as a persistent grid (one CTA per
+// SM walking the query tiles).  With few key tiles per query tile, the
+// per-tile setup and epilogue that the persistent form overlaps weigh more.
+#ifndef DIFFATTN_PERSIST_MAX_NK
+#define DIFFATTN_PERSIST_MAX_NK 4096
+#endif
+static constexpr int kPersistMaxNk = DIFFATTN_PERSIST_MAX_NK;
+
 template <int D, int DV, bool CAUSAL, bool QK8>
 static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     using L = PrefillLayout<D, DV, QK8>;
@@ -118,11 +140,14 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     p.o2 = a.o2;
     p.lse = a.lse;
     p.qk_scale = a.qk_scale;
-    auto kern = prefill_kernel<D, DV, CAUSAL, QK8>;
+    const long long tiles = (long long)((a.Nq + L::BM - 1) / L::BM) * a.H * a.B;
+    const int sms = sm_count();
+    const bool persist = sms > 0 && tiles > sms && a.Nk <= kPersistMaxNk;
+    auto kern = persist ? prefill_kernel<D, DV, CAUSAL, QK8, true> : prefill_kernel<D, DV, CAUSAL, QK8, false>;
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
                  "prefill: set shared memory"))
         return LAUNCH_ERR_CUDA;
-    const dim3 grid((a.Nq + L::BM - 1) / L::BM, a.H, a.B);
+    const dim3 grid = persist ? dim3(sms, 1, 1) : dim3((a.Nq + L::BM - 1) / L::BM, a.H, a.B);
     kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq1, mq2, mk1, mk2, mv, p);
     return cuda_ok(cudaGetLastError(), "prefill: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }

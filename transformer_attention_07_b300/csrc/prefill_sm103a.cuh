@@ -14,7 +14,11 @@
 //
 // One CTA owns a tile of 128 query rows of one (b, h) and walks the key tiles
 // (128 keys each; under causal masking only the tiles at or left of the
-// diagonal).  Warp roles:
+// diagonal).  In the persistent form (PERSIST) a grid of one CTA per SM walks
+// the query tiles in heaviest-first order, each CTA taking every G-th tile in
+// alternating direction (G = grid size); the key/value rings and barrier
+// phases run on across tiles, so the next tile's Q load and first scores
+// overlap the current tile's epilogue.  Warp roles:
 //   warp 0       TMA producer: Q1/Q2 once, then K1/K2 and V tiles into
 //                shared-memory rings (128-byte swizzle).
 //   warp 1       tensor-core issuer (one thread) and TMEM owner:
@@ -81,7 +85,10 @@ struct PrefillLayout {
     static constexpr int B_SFULL = B_VEMPTY + VST;   // 2 (one per map)
     static constexpr int B_PFULL = B_SFULL + 2;      // 2
     static constexpr int B_OFULL = B_PFULL + 2;
-    static constexpr int NBAR = B_OFULL + 1;
+    static constexpr int B_OFREE = B_OFULL + 1;      // persistent: O read by the epilogue (count 256)
+    static constexpr int B_QEMPTY = B_OFREE + 1;     // persistent: Q tiles no longer read
+    static constexpr int B_DRAIN = B_QEMPTY + 1;     // issuer: every issued MMA complete (error path)
+    static constexpr int NBAR = B_DRAIN + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
     static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
     // +1024 for aligning the dynamic base; at least 120 KB so that a single
@@ -99,7 +106,7 @@ struct PrefillLayout {
     static_assert(USED + 1024 <= 227u * 1024u, "shared memory");
 };
 
-template <int D, int DV, bool CAUSAL, bool QK8 = false>
+template <int D, int DV, bool CAUSAL, bool QK8 = false, bool PERSIST = false>
 __global__ void __launch_bounds__(384, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
                const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
@@ -111,15 +118,34 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // Tile: heaviest (right-most under causal masking) query tiles first.
+    // Tiles: heaviest (right-most under causal masking) query tiles first.
+    // Without PERSIST the CTA owns tile (blockIdx.x, y, z); with it, tile
+    // number t = k G + (k even ? c : G - 1 - c) of the (b, h)-major,
+    // heaviest-first order for k = 0, 1, ... (c = blockIdx.x, G = gridDim.x).
     const int num_qt = (p.Nq + L::BM - 1) / L::BM;
-    const int qt = num_qt - 1 - (int)blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int q0 = qt * L::BM;
     const int diag = p.Nk - p.Nq;   // key j visible to query i iff j <= i + diag (causal)
-    int kv_end = p.Nk;
-    if (CAUSAL) kv_end = min(p.Nk, q0 + L::BM + diag);
-    const int n_kv = (kv_end + L::BN - 1) / L::BN;
+    auto tile = [&](int k, int& qt, int& h, int& b) -> bool {
+        if constexpr (!PERSIST) {
+            qt = num_qt - 1 - (int)blockIdx.x;
+            h = blockIdx.y;
+            b = blockIdx.z;
+            return k == 0;
+        } else {
+            const long long G = gridDim.x, c = blockIdx.x;
+            const long long t = (long long)k * G + ((k & 1) ? G - 1 - c : c);
+            if (t >= (long long)num_qt * p.H * p.B) return false;
+            const long long bh = t / num_qt;
+            qt = num_qt - 1 - (int)(t - bh * num_qt);
+            h = (int)(bh % p.H);
+            b = (int)(bh / p.H);
+            return true;
+        }
+    };
+    auto kv_tiles = [&](int qt) -> int {
+        int kv_end = p.Nk;
+        if (CAUSAL) kv_end = min(p.Nk, qt * L::BM + L::BM + diag);
+        return (kv_end + L::BN - 1) / L::BN;
+    };
 
     auto bar = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)i; };
 
@@ -138,6 +164,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             mbar_init(bar(L::B_PFULL + r), 128);
         }
         mbar_init(bar(L::B_OFULL), 1);
+        mbar_init(bar(L::B_OFREE), 256);
+        mbar_init(bar(L::B_QEMPTY), 1);
+        mbar_init(bar(L::B_DRAIN), 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_q1);
         prefetch_tensormap(&tm_q2);
@@ -158,32 +187,45 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             bool ok = true;
-            mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::Q_BYTES);
-            tma_load_4d(sb + L::OFF_Q1, &tm_q1, bar(L::B_Q), 0, q0, h, b);
-            tma_load_4d(sb + L::OFF_Q2, &tm_q2, bar(L::B_Q), 0, q0, h, b);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int ks = j % L::KST;
-                ok = mbar_wait(bar(L::B_KEMPTY + ks), ((j / L::KST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
-                if (!ok) break;
-                const uint32_t k1s = sb + L::OFF_K + (uint32_t)ks * 2 * L::K_BYTES;
-                mbar_arrive_expect_tx(bar(L::B_KFULL + ks), 2 * L::K_BYTES);
-                tma_load_4d(k1s, &tm_k1, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
-                tma_load_4d(k1s + L::K_BYTES, &tm_k2, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
-                ++k_issued;
-                const int vs = j % L::VST;
-                ok = mbar_wait(bar(L::B_VEMPTY + vs), ((j / L::VST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
-                if (!ok) break;
-                const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
-                mbar_arrive_expect_tx(bar(L::B_VFULL + vs), L::V_BYTES);
+            // Stage counters run on across query tiles: the g-th key tile of
+            // the CTA uses ring stage g % depth in phase (g / depth) & 1.
+            int k_issued = 0, v_issued = 0, q_issued = 0;
+            int qt, h, b;
+            for (int k = 0; ok && tile(k, qt, h, b); ++k) {
+                if (k > 0) {
+                    ok = mbar_wait(bar(L::B_QEMPTY), (k - 1) & 1, ERR_SITE_PREFILL_PRODUCER);
+                    if (!ok) break;
+                }
+                mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::Q_BYTES);
+                tma_load_4d(sb + L::OFF_Q1, &tm_q1, bar(L::B_Q), 0, qt * L::BM, h, b);
+                tma_load_4d(sb + L::OFF_Q2, &tm_q2, bar(L::B_Q), 0, qt * L::BM, h, b);
+                ++q_issued;
+                const int n_kv = kv_tiles(qt);
+                for (int j = 0; j < n_kv; ++j) {
+                    const int ks = k_issued % L::KST;
+                    ok = mbar_wait(bar(L::B_KEMPTY + ks), ((k_issued / L::KST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
+                    if (!ok) break;
+                    const uint32_t k1s = sb + L::OFF_K + (uint32_t)ks * 2 * L::K_BYTES;
+                    mbar_arrive_expect_tx(bar(L::B_KFULL + ks), 2 * L::K_BYTES);
+                    tma_load_4d(k1s, &tm_k1, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
+                    tma_load_4d(k1s + L::K_BYTES, &tm_k2, bar(L::B_KFULL + ks), 0, j * L::BN, h, b);
+                    ++k_issued;
+                    const int vs = v_issued % L::VST;
+                    ok = mbar_wait(bar(L::B_VEMPTY + vs), ((v_issued / L::VST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
+                    if (!ok) break;
+                    const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
+                    mbar_arrive_expect_tx(bar(L::B_VFULL + vs), L::V_BYTES);
 #pragma unroll
-                for (int c = 0; c < DV / 64; ++c)
-                    tma_load_4d(vsm + (uint32_t)c * L::V_BOX, &tm_v, bar(L::B_VFULL + vs), c * 64, j * L::BN, h, b);
-                ++v_issued;
+                    for (int c = 0; c < DV / 64; ++c)
+                        tma_load_4d(vsm + (uint32_t)c * L::V_BOX, &tm_v, bar(L::B_VFULL + vs), c * 64, j * L::BN, h,
+                                    b);
+                    ++v_issued;
+                }
+                if constexpr (!PERSIST) break;
             }
             // Never leave with copies in flight: wait (bounded) for the last
             // phase armed on every stage.
-            mbar_wait(bar(L::B_Q), 0, ERR_SITE_PREFILL_DRAIN);
+            if (q_issued > 0) mbar_wait(bar(L::B_Q), (q_issued - 1) & 1, ERR_SITE_PREFILL_DRAIN);
             for (int s = 0; s < L::KST && s < k_issued; ++s) {
                 const int last = s + ((k_issued - 1 - s) / L::KST) * L::KST;
                 mbar_wait(bar(L::B_KFULL + s), (last / L::KST) & 1, ERR_SITE_PREFILL_DRAIN);
@@ -228,50 +270,77 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                         mma_ss(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk, k > 0 ? 1u : 0u);
                 }
             };
-            for (int j = 0; j <= n_kv && ok; ++j) {
-                const int ks = j % L::KST;
-                if (j < n_kv) {
-                    ok = mbar_wait(bar(L::B_KFULL + ks), (j / L::KST) & 1, ERR_SITE_PREFILL_MMA);
+            int g = 0;   // key tiles of earlier query tiles (ring stage and phase counter)
+            int qt, h, b;
+            for (int k = 0; ok && tile(k, qt, h, b); ++k) {
+                const int n_kv = kv_tiles(qt);
+                if (k > 0) {
+                    ok = mbar_wait(bar(L::B_Q), k & 1, ERR_SITE_PREFILL_MMA);
                     if (!ok) break;
                     tc_fence_after();
                 }
-                const int jv = j - 1;
-                const int vs = (jv + L::VST) % L::VST;
-                if (jv >= 0) {
-                    ok = mbar_wait(bar(L::B_VFULL + vs), (jv / L::VST) & 1, ERR_SITE_PREFILL_MMA);
-                    if (!ok) break;
+                for (int j = 0; j <= n_kv; ++j) {
+                    const int gj = g + j;
+                    const int ks = gj % L::KST;
+                    if (j < n_kv) {
+                        ok = mbar_wait(bar(L::B_KFULL + ks), (gj / L::KST) & 1, ERR_SITE_PREFILL_MMA);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    const int jv = j - 1, gv = gj - 1;
+                    const int vs = (gv + L::VST) % L::VST;
+                    if (jv >= 0) {
+                        ok = mbar_wait(bar(L::B_VFULL + vs), (gv / L::VST) & 1, ERR_SITE_PREFILL_MMA);
+                        if (!ok) break;
+                    }
+                    const uint64_t dvs = dv0 + (uint64_t)vs * VSTAGE;
+                    const uint64_t dks = dk0 + (uint64_t)ks * KSTAGE;
+                    const uint32_t acc0 = jv > 0 ? 1u : 0u;
+                    // map 1: O1 += P1 V (previous tile), then S1 = Q1 K1^T (this tile)
+                    if (jv >= 0) {
+                        ok = mbar_wait(bar(L::B_PFULL + 0), gv & 1, ERR_SITE_PREFILL_MMA);
+                        if (!ok) break;
+                        if (PERSIST && jv == 0 && k > 0) {
+                            // The first product of a query tile overwrites O:
+                            // the previous tile's epilogue must have read it.
+                            ok = mbar_wait(bar(L::B_OFREE), (k - 1) & 1, ERR_SITE_PREFILL_MMA);
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+                        pv(t_o1, t_s1, dvs, acc0);
+                    }
+                    if (j < n_kv) {
+                        qk(t_s1, dq1, dks);
+                        mma_commit(bar(L::B_SFULL + 0));
+                    }
+                    // map 2
+                    if (jv >= 0) {
+                        ok = mbar_wait(bar(L::B_PFULL + 1), gv & 1, ERR_SITE_PREFILL_MMA);
+                        if (!ok) break;
+                        tc_fence_after();
+                        pv(t_o2, t_s2, dvs, acc0);
+                        mma_commit(bar(L::B_VEMPTY + vs));
+                    }
+                    if (j < n_kv) {
+                        qk(t_s2, dq2, dks + K2_OFF);
+                        mma_commit(bar(L::B_SFULL + 1));
+                        mma_commit(bar(L::B_KEMPTY + ks));
+                        if (PERSIST && j == n_kv - 1) mma_commit(bar(L::B_QEMPTY));
+                    }
                 }
-                const uint64_t dvs = dv0 + (uint64_t)vs * VSTAGE;
-                const uint64_t dks = dk0 + (uint64_t)ks * KSTAGE;
-                const uint32_t acc0 = jv > 0 ? 1u : 0u;
-                // map 1: O1 += P1 V (previous tile), then S1 = Q1 K1^T (this tile)
-                if (jv >= 0) {
-                    ok = mbar_wait(bar(L::B_PFULL + 0), jv & 1, ERR_SITE_PREFILL_MMA);
-                    if (!ok) break;
-                    tc_fence_after();
-                    pv(t_o1, t_s1, dvs, acc0);
-                }
-                if (j < n_kv) {
-                    qk(t_s1, dq1, dks);
-                    mma_commit(bar(L::B_SFULL + 0));
-                }
-                // map 2
-                if (jv >= 0) {
-                    ok = mbar_wait(bar(L::B_PFULL + 1), jv & 1, ERR_SITE_PREFILL_MMA);
-                    if (!ok) break;
-                    tc_fence_after();
-                    pv(t_o2, t_s2, dvs, acc0);
-                    mma_commit(bar(L::B_VEMPTY + vs));
-                }
-                if (j < n_kv) {
-                    qk(t_s2, dq2, dks + K2_OFF);
-                    mma_commit(bar(L::B_SFULL + 1));
-                    mma_commit(bar(L::B_KEMPTY + ks));
-                }
+                g += n_kv;
+                // The epilogue of this query tile may start once every MMA
+                // issued so far has completed.
+                if (ok) mma_commit(bar(L::B_OFULL));
+                if constexpr (!PERSIST) break;
             }
-            // Always signal the epilogue (also after a failed wait) once every
-            // MMA issued so far has completed.
-            mma_commit(bar(L::B_OFULL));
+            if (!ok) {
+                // Error: signal the epilogue anyway, and let no MMA outlive
+                // the kernel's tensor memory.
+                mma_commit(bar(L::B_OFULL));
+                mma_commit(bar(L::B_DRAIN));
+                mbar_wait(bar(L::B_DRAIN), 0, ERR_SITE_PREFILL_DRAIN);
+            }
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -282,16 +351,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
         const uint32_t s_col = r ? L::TM_S2 : L::TM_S1;
         const uint32_t o_col = r ? L::TM_O2 : L::TM_O1;
-        const int qi = q0 + row;
+        bool ok = true;
+        int g = 0;   // key tiles of earlier query tiles (barrier phase counter)
+        int qt, h, b;
+        for (int k = 0; ok && tile(k, qt, h, b); ++k) {
+        const int n_kv = kv_tiles(qt);
+        const int qi = qt * L::BM + row;
         const int kmax = CAUSAL ? min(qi + diag, p.Nk - 1) : p.Nk - 1;   // last visible key
         // log2(e)/sqrt(d), times the map's q and k dequantisation scales.
         float sl2 = p.scale_log2;
         if constexpr (QK8) sl2 *= p.qk_scale[(2 * r) * p.H + h] * p.qk_scale[(2 * r + 1) * p.H + h];
         float m = -INFINITY;   // running max of scaled logits (log2 domain)
         float l = 0.f;         // running sum of the bf16-rounded probabilities
-        bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            ok = mbar_wait(bar(L::B_SFULL + r), j & 1, ERR_SITE_PREFILL_SOFTMAX);
+            ok = mbar_wait(bar(L::B_SFULL + r), (g + j) & 1, ERR_SITE_PREFILL_SOFTMAX);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -368,7 +441,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         }
 
         // ------------------------------------------------------------ epilogue
-        mbar_wait(bar(L::B_OFULL), 0, ERR_SITE_PREFILL_EPILOGUE);
+        g += n_kv;
+        if (!mbar_wait(bar(L::B_OFULL), k & 1, ERR_SITE_PREFILL_EPILOGUE)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);
         __syncwarp();
         tc_fence_after();
         float* epi = reinterpret_cast<float*>(smem + L::OFF_EPI);
@@ -411,6 +486,11 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 // contraction), so identical maps with lambda = 1 cancel to 0.
                 o[32 * c + i] = __fmul_rn(__uint_as_float(a[i]), inv1) - __fmul_rn(__uint_as_float(bb[i]), inv2);
         }
+        if constexpr (PERSIST) {
+            // O1, O2 are in registers: the next tile's products may overwrite them.
+            tc_fence_before();
+            mbar_arrive(bar(L::B_OFREE));
+        }
         float sum = 0.f;
 #pragma unroll
         for (int i = 0; i < HALF; ++i) sum += o[i];
@@ -441,6 +521,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                                     pack_bf16x2(y[6], y[7]));
             }
         }
+        if constexpr (!PERSIST) break;
+        }   // query tiles
     }
 
     tc_fence_before();

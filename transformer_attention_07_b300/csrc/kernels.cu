@@ -290,11 +290,15 @@ static int launch_standard_t(const StandardArgs& a, cudaStream_t st) {
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)L::D));
     p.out = static_cast<uint16_t*>(a.out);
     p.out_f32 = a.out_f32;
-    auto kern = standard_attn_kernel<CAUSAL>;
+    // Persistent for short sequences, as the differential prefill.
+    const long long pairs = (long long)((a.Nq + 2 * L::BM - 1) / (2 * L::BM)) * a.H * a.B;
+    const int sms = sm_count();
+    const bool persist = sms > 0 && pairs > sms && a.Nk <= kPersistMaxNk;
+    auto kern = persist ? standard_attn_kernel<CAUSAL, true> : standard_attn_kernel<CAUSAL, false>;
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
                  "standard attention: set shared memory"))
         return LAUNCH_ERR_CUDA;
-    const dim3 grid((a.Nq + 2 * L::BM - 1) / (2 * L::BM), a.H, a.B);
+    const dim3 grid = persist ? dim3(sms, 1, 1) : dim3((a.Nq + 2 * L::BM - 1) / (2 * L::BM), a.H, a.B);
     kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq, mk, mv, p);
     return cuda_ok(cudaGetLastError(), "standard attention: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }

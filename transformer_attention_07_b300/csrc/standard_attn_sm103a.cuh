@@ -13,7 +13,9 @@
 //
 // One CTA owns two 128-row query tiles of one (b, h) (rows q0 .. q0+255),
 // which share every K and V tile; they take the places of the two maps of
-// the differential kernel.  Warp roles:
+// the differential kernel.  As in the differential kernel, a persistent form
+// (PERSIST) walks such tile pairs with one CTA per SM for short sequences.
+// Warp roles:
 //   warp 0       TMA producer: both Q tiles once, then K and V tiles.
 //   warp 1       tensor-core issuer: per key tile and query tile r,
 //                O_r += P_r V (previous key tile, A = P in TMEM) then
@@ -58,7 +60,10 @@ struct StandardLayout {
     static constexpr int B_SFULL = B_VEMPTY + VST;   // [tile]
     static constexpr int B_PFULL = B_SFULL + 2;      // [tile]
     static constexpr int B_OFULL = B_PFULL + 2;
-    static constexpr int NBAR = B_OFULL + 1;
+    static constexpr int B_OFREE = B_OFULL + 1;      // persistent: O read by the epilogue (count 256)
+    static constexpr int B_QEMPTY = B_OFREE + 1;     // persistent: Q tiles no longer read
+    static constexpr int B_DRAIN = B_QEMPTY + 1;     // issuer: every issued MMA complete (error path)
+    static constexpr int NBAR = B_DRAIN + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
     static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
     static constexpr uint32_t SMEM_BYTES = USED + 1024;
@@ -68,7 +73,7 @@ struct StandardLayout {
     static_assert(USED + 1024 <= 227u * 1024u, "shared memory");
 };
 
-template <bool CAUSAL>
+template <bool CAUSAL, bool PERSIST = false>
 __global__ void __launch_bounds__(384, 1)
 standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const StandardParams p) {
@@ -80,14 +85,33 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int lane = threadIdx.x & 31;
 
     // Two query tiles per CTA; heaviest pairs first under causal masking.
+    // Without PERSIST the CTA owns pair (blockIdx.x, y, z); with it, pair
+    // number t = k G + (k even ? c : G - 1 - c) of the (b, h)-major,
+    // heaviest-first order for k = 0, 1, ... (c = blockIdx.x, G = gridDim.x).
     const int num_pairs = (p.Nq + 2 * L::BM - 1) / (2 * L::BM);
-    const int pr = num_pairs - 1 - (int)blockIdx.x;
-    const int h = blockIdx.y, b = blockIdx.z;
-    const int q0 = pr * 2 * L::BM;
     const int diag = p.Nk - p.Nq;
-    int kv_end = p.Nk;
-    if (CAUSAL) kv_end = min(p.Nk, q0 + 2 * L::BM + diag);
-    const int n_kv = (kv_end + L::BN - 1) / L::BN;
+    auto tile = [&](int k, int& pr, int& h, int& b) -> bool {
+        if constexpr (!PERSIST) {
+            pr = num_pairs - 1 - (int)blockIdx.x;
+            h = blockIdx.y;
+            b = blockIdx.z;
+            return k == 0;
+        } else {
+            const long long G = gridDim.x, c = blockIdx.x;
+            const long long t = (long long)k * G + ((k & 1) ? G - 1 - c : c);
+            if (t >= (long long)num_pairs * p.H * p.B) return false;
+            const long long bh = t / num_pairs;
+            pr = num_pairs - 1 - (int)(t - bh * num_pairs);
+            h = (int)(bh % p.H);
+            b = (int)(bh / p.H);
+            return true;
+        }
+    };
+    auto kv_tiles = [&](int pr) -> int {
+        int kv_end = p.Nk;
+        if (CAUSAL) kv_end = min(p.Nk, pr * 2 * L::BM + 2 * L::BM + diag);
+        return (kv_end + L::BN - 1) / L::BN;
+    };
 
     auto bar = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)i; };
 
@@ -106,6 +130,9 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             mbar_init(bar(L::B_PFULL + r), 4);   // one elected lane per softmax warp
         }
         mbar_init(bar(L::B_OFULL), 1);
+        mbar_init(bar(L::B_OFREE), 256);
+        mbar_init(bar(L::B_QEMPTY), 1);
+        mbar_init(bar(L::B_DRAIN), 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
@@ -124,35 +151,47 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             bool ok = true;
-            mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::Q_BYTES);
+            // Stage counters run on across tile pairs.
+            int k_issued = 0, v_issued = 0, q_issued = 0;
+            int pr, h, b;
+            for (int k = 0; ok && tile(k, pr, h, b); ++k) {
+                if (k > 0) {
+                    ok = mbar_wait(bar(L::B_QEMPTY), (k - 1) & 1, ERR_SITE_PREFILL_PRODUCER);
+                    if (!ok) break;
+                }
+                const int q0 = pr * 2 * L::BM;
+                mbar_arrive_expect_tx(bar(L::B_Q), 2 * L::Q_BYTES);
 #pragma unroll
-            for (int r = 0; r < 2; ++r)
+                for (int r = 0; r < 2; ++r)
 #pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    tma_load_4d(sb + L::OFF_Q + (uint32_t)r * L::Q_BYTES + (uint32_t)a * L::ATOM, &tm_q, bar(L::B_Q),
-                                a * 64, q0 + r * L::BM, h, b);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int ks = j % L::KST;
-                ok = mbar_wait(bar(L::B_KEMPTY + ks), ((j / L::KST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
-                if (!ok) break;
-                const uint32_t kst = sb + L::OFF_K + (uint32_t)ks * L::K_BYTES;
-                mbar_arrive_expect_tx(bar(L::B_KFULL + ks), L::K_BYTES);
+                    for (int a = 0; a < 2; ++a)
+                        tma_load_4d(sb + L::OFF_Q + (uint32_t)r * L::Q_BYTES + (uint32_t)a * L::ATOM, &tm_q,
+                                    bar(L::B_Q), a * 64, q0 + r * L::BM, h, b);
+                ++q_issued;
+                const int n_kv = kv_tiles(pr);
+                for (int j = 0; j < n_kv; ++j) {
+                    const int ks = k_issued % L::KST;
+                    ok = mbar_wait(bar(L::B_KEMPTY + ks), ((k_issued / L::KST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
+                    if (!ok) break;
+                    const uint32_t kst = sb + L::OFF_K + (uint32_t)ks * L::K_BYTES;
+                    mbar_arrive_expect_tx(bar(L::B_KFULL + ks), L::K_BYTES);
 #pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    tma_load_4d(kst + (uint32_t)a * L::ATOM, &tm_k, bar(L::B_KFULL + ks), a * 64, j * L::BN, h, b);
-                ++k_issued;
-                const int vs = j % L::VST;
-                ok = mbar_wait(bar(L::B_VEMPTY + vs), ((j / L::VST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
-                if (!ok) break;
-                const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
-                mbar_arrive_expect_tx(bar(L::B_VFULL + vs), L::V_BYTES);
+                    for (int a = 0; a < 2; ++a)
+                        tma_load_4d(kst + (uint32_t)a * L::ATOM, &tm_k, bar(L::B_KFULL + ks), a * 64, j * L::BN, h, b);
+                    ++k_issued;
+                    const int vs = v_issued % L::VST;
+                    ok = mbar_wait(bar(L::B_VEMPTY + vs), ((v_issued / L::VST) & 1) ^ 1, ERR_SITE_PREFILL_PRODUCER);
+                    if (!ok) break;
+                    const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
+                    mbar_arrive_expect_tx(bar(L::B_VFULL + vs), L::V_BYTES);
 #pragma unroll
-                for (int a = 0; a < 2; ++a)
-                    tma_load_4d(vsm + (uint32_t)a * L::ATOM, &tm_v, bar(L::B_VFULL + vs), a * 64, j * L::BN, h, b);
-                ++v_issued;
+                    for (int a = 0; a < 2; ++a)
+                        tma_load_4d(vsm + (uint32_t)a * L::ATOM, &tm_v, bar(L::B_VFULL + vs), a * 64, j * L::BN, h, b);
+                    ++v_issued;
+                }
+                if constexpr (!PERSIST) break;
             }
-            mbar_wait(bar(L::B_Q), 0, ERR_SITE_PREFILL_DRAIN);
+            if (q_issued > 0) mbar_wait(bar(L::B_Q), (q_issued - 1) & 1, ERR_SITE_PREFILL_DRAIN);
             for (int s = 0; s < L::KST && s < k_issued; ++s) {
                 const int last = s + ((k_issued - 1 - s) / L::KST) * L::KST;
                 mbar_wait(bar(L::B_KFULL + s), (last / L::KST) & 1, ERR_SITE_PREFILL_DRAIN);
@@ -172,25 +211,41 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_after();
             const uint32_t s_col[2] = {L::TM_S0, L::TM_S1};
             const uint32_t o_col[2] = {L::TM_O0, L::TM_O1};
+            int g = 0;   // key tiles of earlier tile pairs (ring stage and phase counter)
+            int pr, h, b;
+            for (int k = 0; ok && tile(k, pr, h, b); ++k) {
+            const int n_kv = kv_tiles(pr);
+            if (k > 0) {
+                ok = mbar_wait(bar(L::B_Q), k & 1, ERR_SITE_PREFILL_MMA);
+                if (!ok) break;
+                tc_fence_after();
+            }
             for (int j = 0; j <= n_kv && ok; ++j) {
-                const int ks = j % L::KST;
+                const int gj = g + j;
+                const int ks = gj % L::KST;
                 if (j < n_kv) {
-                    ok = mbar_wait(bar(L::B_KFULL + ks), (j / L::KST) & 1, ERR_SITE_PREFILL_MMA);
+                    ok = mbar_wait(bar(L::B_KFULL + ks), (gj / L::KST) & 1, ERR_SITE_PREFILL_MMA);
                     if (!ok) break;
                     tc_fence_after();
                 }
-                const int jv = j - 1;
-                const int vs = (jv + L::VST) % L::VST;
+                const int jv = j - 1, gv = gj - 1;
+                const int vs = (gv + L::VST) % L::VST;
                 if (jv >= 0) {
-                    ok = mbar_wait(bar(L::B_VFULL + vs), (jv / L::VST) & 1, ERR_SITE_PREFILL_MMA);
+                    ok = mbar_wait(bar(L::B_VFULL + vs), (gv / L::VST) & 1, ERR_SITE_PREFILL_MMA);
                     if (!ok) break;
                 }
                 const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
                 const uint32_t kst = sb + L::OFF_K + (uint32_t)ks * L::K_BYTES;
                 for (int r = 0; r < 2; ++r) {
                     if (jv >= 0) {
-                        ok = mbar_wait(bar(L::B_PFULL + r), jv & 1, ERR_SITE_PREFILL_MMA);
+                        ok = mbar_wait(bar(L::B_PFULL + r), gv & 1, ERR_SITE_PREFILL_MMA);
                         if (!ok) break;
+                        if (PERSIST && jv == 0 && r == 0 && k > 0) {
+                            // The first product of a tile pair overwrites O:
+                            // the previous pair's epilogue must have read it.
+                            ok = mbar_wait(bar(L::B_OFREE), (k - 1) & 1, ERR_SITE_PREFILL_MMA);
+                            if (!ok) break;
+                        }
                         tc_fence_after();
 #pragma unroll
                         for (int k = 0; k < L::BN / 16; ++k) {
@@ -211,10 +266,21 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                         }
                         mma_commit(bar(L::B_SFULL + r));
                         if (r == 1) mma_commit(bar(L::B_KEMPTY + ks));
+                        if (PERSIST && r == 1 && j == n_kv - 1) mma_commit(bar(L::B_QEMPTY));
                     }
                 }
             }
-            mma_commit(bar(L::B_OFULL));
+            g += n_kv;
+            if (ok) mma_commit(bar(L::B_OFULL));
+            if constexpr (!PERSIST) break;
+            }
+            if (!ok) {
+                // Error: signal the epilogue anyway, and let no MMA outlive
+                // the kernel's tensor memory.
+                mma_commit(bar(L::B_OFULL));
+                mma_commit(bar(L::B_DRAIN));
+                mbar_wait(bar(L::B_DRAIN), 0, ERR_SITE_PREFILL_DRAIN);
+            }
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -225,14 +291,18 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
         const uint32_t s_col = r ? L::TM_S1 : L::TM_S0;
         const uint32_t o_col = r ? L::TM_O1 : L::TM_O0;
-        const int qi = q0 + r * L::BM + row;
-        const int kmax = CAUSAL ? min(qi + diag, p.Nk - 1) : p.Nk - 1;
         const float sl2 = p.scale_log2;
+        bool ok = true;
+        int g = 0;   // key tiles of earlier tile pairs (barrier phase counter)
+        int pr, h, b;
+        for (int k = 0; ok && tile(k, pr, h, b); ++k) {
+        const int n_kv = kv_tiles(pr);
+        const int qi = pr * 2 * L::BM + r * L::BM + row;
+        const int kmax = CAUSAL ? min(qi + diag, p.Nk - 1) : p.Nk - 1;
         float m = -INFINITY;
         float l = 0.f;
-        bool ok = true;
         for (int j = 0; j < n_kv; ++j) {
-            ok = mbar_wait(bar(L::B_SFULL + r), j & 1, ERR_SITE_PREFILL_SOFTMAX);
+            ok = mbar_wait(bar(L::B_SFULL + r), (g + j) & 1, ERR_SITE_PREFILL_SOFTMAX);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
@@ -302,8 +372,9 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
 
         // ------------------------------------------------------------ epilogue: out = O_r / l_r
-        mbar_wait(bar(L::B_OFULL), 0, ERR_SITE_PREFILL_EPILOGUE);
-        __syncwarp();
+        g += n_kv;
+        if (!mbar_wait(bar(L::B_OFULL), k & 1, ERR_SITE_PREFILL_EPILOGUE)) ok = false;
+        ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         const float inv = 1.0f / l;
 #pragma unroll
@@ -327,6 +398,13 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                                         pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7]));
             }
         }
+        if constexpr (PERSIST) {
+            // O has been read: the next pair's products may overwrite it.
+            tc_fence_before();
+            mbar_arrive(bar(L::B_OFREE));
+        }
+        if constexpr (!PERSIST) break;
+        }   // tile pairs
     }
 
     tc_fence_before();

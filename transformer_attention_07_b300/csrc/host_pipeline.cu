@@ -2,7 +2,10 @@
 // staging of a host-to-host call.  The B*H heads are cut into chunks of whole
 // heads; each chunk moves through three stages on three streams:
 //   copy-in stream    q1, k1, q2, k2, v of the chunk, host -> device slot
-//   caller's stream   the prefill kernel on that slot
+//   compute streams   the prefill kernel on that slot, alternating between
+//                     the caller's stream and a second one, so that a
+//                     chunk's kernel starts filling SMs while the previous
+//                     chunk's last CTAs are still running
 //   copy-out stream   the chunk's output, device slot -> host
 // A ring of device slots (in the caller's workspace) lets chunk i's copy-in
 // overlap chunk i-1's kernel and chunk i-2's copy-out, so the transfers hide
@@ -56,7 +59,7 @@ int chunk_heads(int B, int H, int heads_per_chunk) {
 // Streams and events of one call, released when the call returns (the
 // runtime defers the release of objects whose work is still pending).
 struct Pipeline {
-    cudaStream_t in = nullptr, out = nullptr;
+    cudaStream_t in = nullptr, out = nullptr, comp = nullptr;
     cudaEvent_t start = nullptr, end = nullptr;
     cudaEvent_t loaded[kSlots] = {}, computed[kSlots] = {}, drained[kSlots] = {};
     bool ok = true;
@@ -64,6 +67,7 @@ struct Pipeline {
     Pipeline() {
         ok = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking) == cudaSuccess &&
              cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking) == cudaSuccess &&
+             cudaStreamCreateWithFlags(&comp, cudaStreamNonBlocking) == cudaSuccess &&
              cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess &&
              cudaEventCreateWithFlags(&end, cudaEventDisableTiming) == cudaSuccess;
         for (int s = 0; s < kSlots && ok; ++s)
@@ -81,6 +85,7 @@ struct Pipeline {
         if (end) cudaEventDestroy(end);
         if (in) cudaStreamDestroy(in);
         if (out) cudaStreamDestroy(out);
+        if (comp) cudaStreamDestroy(comp);
     }
 };
 
@@ -117,7 +122,8 @@ int diffattn_fwd_host(const void* q1, const void* k1, const void* q2, const void
     if (!pl.ok) return DIFFATTN_ERR_CUDA;
     // The copies start after the caller's earlier work on its stream.
     if (cudaEventRecord(pl.start, cs) != cudaSuccess || cudaStreamWaitEvent(pl.in, pl.start, 0) != cudaSuccess ||
-        cudaStreamWaitEvent(pl.out, pl.start, 0) != cudaSuccess)
+        cudaStreamWaitEvent(pl.out, pl.start, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(pl.comp, pl.start, 0) != cudaSuccess)
         return DIFFATTN_ERR_CUDA;
 
     const size_t qh = (size_t)Nq * d * 2, kh = (size_t)Nk * d * 2, vh = (size_t)Nk * dv * 2, oh = (size_t)Nq * dv * 2;
@@ -140,18 +146,20 @@ int diffattn_fwd_host(const void* q1, const void* k1, const void* q2, const void
             ok = ok && cudaMemcpyAsync(dk2, host(k2, head * kh), hc * kh, cudaMemcpyHostToDevice, pl.in) == cudaSuccess;
             ok = ok && cudaMemcpyAsync(dvs, host(v, head * vh), hc * vh, cudaMemcpyHostToDevice, pl.in) == cudaSuccess;
             ok = ok && cudaEventRecord(pl.loaded[s], pl.in) == cudaSuccess;
-            // Kernel: after the inputs landed and the slot's previous output left.
-            ok = ok && cudaStreamWaitEvent(cs, pl.loaded[s], 0) == cudaSuccess;
-            ok = ok && (idx < kSlots || cudaStreamWaitEvent(cs, pl.drained[s], 0) == cudaSuccess);
+            // Kernel: after the inputs landed and the slot's previous output
+            // left; even chunks on the caller's stream, odd ones on the second.
+            cudaStream_t ks = (idx & 1) ? pl.comp : cs;
+            ok = ok && cudaStreamWaitEvent(ks, pl.loaded[s], 0) == cudaSuccess;
+            ok = ok && (idx < kSlots || cudaStreamWaitEvent(ks, pl.drained[s], 0) == cudaSuccess);
             if (!ok) return DIFFATTN_ERR_CUDA;
             diffattn::PrefillArgs a{dq1, dk1, dq2, dk2, dvs, lambda, lambda_init, eps, causal, 1, hc, Nq, Nk, d, dv,
                                     gn_gamma ? gn_gamma + (size_t)h0 * dv : nullptr, dout, nullptr, nullptr,
                                     nullptr, nullptr};
-            const int rc = diffattn::launch_prefill(a, cs);
+            const int rc = diffattn::launch_prefill(a, ks);
             if (rc != diffattn::LAUNCH_OK) return rc == diffattn::LAUNCH_ERR_UNSUPPORTED ? DIFFATTN_ERR_UNSUPPORTED
                                                                                          : DIFFATTN_ERR_CUDA;
             // Copy-out.
-            ok = cudaEventRecord(pl.computed[s], cs) == cudaSuccess &&
+            ok = cudaEventRecord(pl.computed[s], ks) == cudaSuccess &&
                  cudaStreamWaitEvent(pl.out, pl.computed[s], 0) == cudaSuccess &&
                  cudaMemcpyAsync(static_cast<uint8_t*>(out) + head * oh, dout, hc * oh, cudaMemcpyDeviceToHost,
                                  pl.out) == cudaSuccess &&
@@ -159,7 +167,9 @@ int diffattn_fwd_host(const void* q1, const void* k1, const void* q2, const void
             if (!ok) return DIFFATTN_ERR_CUDA;
         }
     }
-    // The caller's stream completes only after the last output has reached the host.
+    // The caller's stream completes only after the last output has reached
+    // the host (the copy-out stream waited for every kernel, on both compute
+    // streams).
     if (cudaEventRecord(pl.end, pl.out) != cudaSuccess || cudaStreamWaitEvent(cs, pl.end, 0) != cudaSuccess)
         return DIFFATTN_ERR_CUDA;
     return DIFFATTN_OK;

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -89,16 +90,19 @@ static bool make_map_bhnd(CUtensorMap* m, const void* base, int B, int H, int N,
 // ----------------------------------------------------------------- prefill
 
 // Streaming multiprocessors of the current device (0 if unknown), cached per
-// device.
+// device; safe to call from several host threads.
 static int sm_count() {
     constexpr int kMaxDevices = 64;
-    static int cache[kMaxDevices] = {};
+    static std::atomic<int> cache[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-    if (dev < kMaxDevices && cache[dev] > 0) return cache[dev];
+    if (dev < kMaxDevices) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev < kMaxDevices) cache[dev] = n;
+    if (dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -288,10 +288,13 @@ int diffattn_decode_merge(const float* partials, int num_parts, int B, int H, in
  * Scratch: the per-split partial softmax states go to one library-owned
  * device array of 8 MiB (8388608 bytes), a file-scope static that every GPU
  * which loads the library holds until the process exits.  A problem needs
- * B*H*splits*2*(dv + 4)*4 bytes of it (splits as chosen for num_splits = 0,
- * or as given); a problem that needs more is rejected with
- * DIFFATTN_ERR_WORKSPACE and nothing is launched.  No call allocates or frees
- * device memory (no cudaMalloc, cudaFree or allocating library routine).
+ * B*H*splits*2*(dv + 4)*4 bytes of it.  With num_splits = 0 the split count
+ * is chosen as diffattn_decode chooses it, but never above the largest count
+ * that fits; DIFFATTN_ERR_WORKSPACE (nothing launched) is returned only when
+ * a single key range per head, or the num_splits the caller fixed, needs more
+ * than 8 MiB.  The arguments are checked before any CUDA runtime call.  No
+ * call allocates or frees device memory (no cudaMalloc, cudaFree or
+ * allocating library routine).
  *
  * Set-up: the first call on a device (with that device current) looks up the
  * array's device address once (cudaGetSymbolAddress) and caches it; make

@@ -59,11 +59,12 @@ size_t workspace_for(int B, int H, int dv, int splits) {
     return (size_t)B * (size_t)H * (size_t)splits * 2u * (size_t)(dv + 4) * sizeof(float);
 }
 
-// Key ranges per (b, h): enough CTAs to fill the GPU in whole waves, and at
-// least 512 keys per range.
-int choose_splits(int64_t heads, int Nk, int sms) {
+// Key ranges per (b, h): enough CTAs to fill the GPU in whole waves, at
+// least 512 keys per range, and at most max_splits ranges.
+int choose_splits(int64_t heads, int Nk, int sms, int max_splits = kMaxAutoSplits) {
     const int by_keys = (int)((Nk + 511) / 512);
-    const int cap = by_keys < kMaxAutoSplits ? (by_keys < 1 ? 1 : by_keys) : kMaxAutoSplits;
+    int cap = by_keys < max_splits ? by_keys : max_splits;
+    if (cap < 1) cap = 1;
     int best = 1;
     double best_eff = -1.0;
     for (int s = 1; s <= cap; ++s) {
@@ -76,6 +77,49 @@ int choose_splits(int64_t heads, int Nk, int sms) {
         }
     }
     return best;
+}
+
+// Streaming multiprocessors of the current device, or 0 if the runtime cannot say.
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (!diffattn::cuda_ok(cudaGetDevice(&dev), "decode: get device") ||
+        !diffattn::cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "decode: SM count"))
+        return 0;
+    return sms;
+}
+
+// Argument checks of the contiguous-cache decode entry points (everything
+// but the workspace); DIFFATTN_OK when the call may proceed.
+int check_decode(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, float lambda,
+                 float lambda_init, int B, int H, int Nk, int d, int dv, const float* gn_gamma, float eps,
+                 int num_splits, const void* out, const float* o_prenorm) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
+    if (num_splits < 0 || num_splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
+    // The key caches are addressed as one [B*H*Nk, d] matrix with 32-bit rows.
+    if ((int64_t)B * H * Nk >= (int64_t(1) << 31) - 64) return DIFFATTN_ERR_INVALID_ARG;
+    return DIFFATTN_OK;
+}
+
+// The launch part of diffattn_decode, once the split count is fixed.
+int decode_with_splits(const void* q1, const void* k1, const void* q2, const void* k2, const void* v, float lambda,
+                       float lambda_init, int B, int H, int Nk, int d, int dv, const float* gn_gamma, float eps,
+                       int splits, void* workspace, size_t workspace_bytes, void* out, float* o_prenorm,
+                       void* stream) {
+    if (!workspace || workspace_bytes < workspace_for(B, H, dv, splits)) return DIFFATTN_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return DIFFATTN_ERR_INVALID_ARG;
+    const int per = (Nk + splits - 1) / splits;
+    const int keys_per_split = (per + 31) / 32 * 32;
+    diffattn::DecodeArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, B, H, Nk, d, dv,
+                           splits, keys_per_split, gn_gamma, static_cast<float*>(workspace), out, o_prenorm,
+                           nullptr, nullptr, 0, 0, 0, false};
+    return from_launch(diffattn::launch_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // namespace
@@ -187,36 +231,18 @@ int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* 
                     float lambda_init, int B, int H, int Nk, int d, int dv, const float* gn_gamma, float eps,
                     int num_splits, void* workspace, size_t workspace_bytes, void* out, float* o_prenorm,
                     void* stream) {
-    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return DIFFATTN_ERR_INVALID_ARG;
-    if (B < 0 || H < 0 || Nk < 1 || d < 1 || dv < 1) return DIFFATTN_ERR_INVALID_ARG;
-    if (num_splits < 0 || num_splits > kMaxSplits) return DIFFATTN_ERR_INVALID_ARG;
-    if (int s = check_scalars(lambda, lambda_init, eps)) return s;
-    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
-    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
-        !aligned16(out) || !aligned16(o_prenorm) || !aligned4(gn_gamma))
-        return DIFFATTN_ERR_INVALID_ARG;
-    if (B > 65535 || H > 65535) return DIFFATTN_ERR_INVALID_ARG;
-    // The key caches are addressed as one [B*H*Nk, d] matrix with 32-bit rows.
-    if ((int64_t)B * H * Nk >= (int64_t(1) << 31) - 64) return DIFFATTN_ERR_INVALID_ARG;
+    if (int s = check_decode(q1, k1, q2, k2, v, lambda, lambda_init, B, H, Nk, d, dv, gn_gamma, eps, num_splits,
+                             out, o_prenorm))
+        return s;
     if ((int64_t)B * H == 0) return DIFFATTN_OK;
     int splits = num_splits;
     if (splits == 0) {
-        int dev = 0, sms = 0;
-        if (!diffattn::cuda_ok(cudaGetDevice(&dev), "decode: get device") ||
-            !diffattn::cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
-                               "decode: SM count") ||
-            sms < 1)
-            return DIFFATTN_ERR_CUDA;
+        const int sms = device_sms();
+        if (sms < 1) return DIFFATTN_ERR_CUDA;
         splits = choose_splits((int64_t)B * H, Nk, sms);
     }
-    if (!workspace || workspace_bytes < workspace_for(B, H, dv, splits)) return DIFFATTN_ERR_WORKSPACE;
-    if (!aligned16(workspace)) return DIFFATTN_ERR_INVALID_ARG;
-    const int per = (Nk + splits - 1) / splits;
-    const int keys_per_split = (per + 31) / 32 * 32;
-    diffattn::DecodeArgs a{q1, k1, q2, k2, v, lambda, lambda_init, eps, B, H, Nk, d, dv,
-                           splits, keys_per_split, gn_gamma, static_cast<float*>(workspace), out, o_prenorm,
-                           nullptr, nullptr, 0, 0, 0, false};
-    return from_launch(diffattn::launch_decode(a, static_cast<cudaStream_t>(stream)));
+    return decode_with_splits(q1, k1, q2, k2, v, lambda, lambda_init, B, H, Nk, d, dv, gn_gamma, eps, splits,
+                              workspace, workspace_bytes, out, o_prenorm, stream);
 }
 
 size_t diffattn_decode_partials_bytes(int B, int H, int dv, int num_splits) {
@@ -264,18 +290,33 @@ int diffattn_decode_merge(const float* partials, int num_parts, int B, int H, in
 }
 
 // Decode for callers that cannot allocate device memory: the split partials
-// go to the library's own static scratch instead of a caller workspace.  All
-// argument checks are those of diffattn_decode; a problem whose partials do
-// not fit the scratch is rejected there with DIFFATTN_ERR_WORKSPACE.
+// go to the library's own static scratch instead of a caller workspace.  The
+// arguments are checked exactly as in diffattn_decode, before the runtime is
+// asked for anything.  With num_splits = 0 the split count is chosen as there
+// but never above what the scratch holds; DIFFATTN_ERR_WORKSPACE only when
+// even one range per head, or the count the caller fixed, does not fit.
 int diffattn_decode_noalloc(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
                             float lambda, float lambda_init, int B, int H, int Nk, int d, int dv,
                             const float* gn_gamma, float eps, int num_splits, void* out, float* o_prenorm,
                             void* stream) {
+    if (int s = check_decode(q1, k1, q2, k2, v, lambda, lambda_init, B, H, Nk, d, dv, gn_gamma, eps, num_splits,
+                             out, o_prenorm))
+        return s;
+    if ((int64_t)B * H == 0) return DIFFATTN_OK;
+    const size_t per_split = workspace_for(B, H, dv, 1);
+    const size_t fit = diffattn::kNoAllocScratchBytes / per_split;
+    if (fit < 1 || (size_t)num_splits > fit) return DIFFATTN_ERR_WORKSPACE;
+    int splits = num_splits;
+    if (splits == 0) {
+        const int sms = device_sms();
+        if (sms < 1) return DIFFATTN_ERR_CUDA;
+        splits = choose_splits((int64_t)B * H, Nk, sms, fit < (size_t)kMaxAutoSplits ? (int)fit : kMaxAutoSplits);
+    }
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
     if (diffattn::decode_noalloc_scratch(&scratch, &scratch_bytes) != diffattn::LAUNCH_OK) return DIFFATTN_ERR_CUDA;
-    return diffattn_decode(q1, k1, q2, k2, v, lambda, lambda_init, B, H, Nk, d, dv, gn_gamma, eps, num_splits,
-                           scratch, scratch_bytes, out, o_prenorm, stream);
+    return decode_with_splits(q1, k1, q2, k2, v, lambda, lambda_init, B, H, Nk, d, dv, gn_gamma, eps, splits,
+                              scratch, scratch_bytes, out, o_prenorm, stream);
 }
 
 int diffattn_decode_paged(const void* q1, const void* q2, const void* k1_pages, const void* k2_pages,

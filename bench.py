@@ -23,7 +23,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -46,20 +45,27 @@ def load_peaks():
         return 1800.0, 1400.0, 6400.0, "fallback"
 
 
-def traffic_from_profiles(kernel_key: str, source: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (its sha256 prefix is recorded beside it)."""
-    path = os.path.join(ROOT, "profiles", "traffic.md")
+def traffic_from_profiles(kernel: str, workload: str, table: str | None = None):
+    """DRAM bytes per launch from the committed ncu record (profiles/traffic.json,
+    or `table`), if it was taken on the current kernel source (its sha256
+    prefix is recorded beside the bytes; source paths are relative to the
+    repository root unless absolute)."""
     try:
-        text = open(path).read()
-        src = open(source, "rb").read()
-    except OSError:
+        with open(table or os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            entries = json.load(f)["entries"]
+    except (OSError, ValueError, KeyError):
         return None
-    sha = hashlib.sha256(src).hexdigest()[:16]
-    m = re.search(rf"^\| {re.escape(kernel_key)} \| (\d+) \| ([0-9a-f]{{16}}) \|", text, re.M)
-    if not m or m.group(2) != sha:
-        return None
-    return int(m.group(1))
+    for e in entries:
+        if e.get("kernel") != kernel or e.get("workload") != workload:
+            continue
+        try:
+            src = open(os.path.join(ROOT, e["source"]), "rb").read()
+        except (OSError, KeyError):
+            return None
+        if hashlib.sha256(src).hexdigest()[:16] != e.get("source_sha256_16"):
+            return None
+        return int(e["bytes_per_launch"])
+    return None
 
 
 class ClockSampler:
@@ -571,7 +577,6 @@ def run_cuda(args, world, rank, local):
         return 0
 
     peak_b, peak_s, peak_hbm, peak_src = load_peaks()
-    csrc = os.path.join(ROOT, "transformer_attention_07_b300", "csrc")
     line = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic"}
@@ -580,8 +585,7 @@ def run_cuda(args, world, rank, local):
         dec_gbs = wd.kv_bytes * args.steps * world / (dec_ms * 1e-3) / 1e9
         dec_roof = {"bound": "hbm", "achieved": dec_gbs / world, "peak": peak_hbm, "unit": "GB/s",
                     "frac": dec_gbs / world / peak_hbm, "peak_source": peak_src,
-                    "traffic": traffic_from_profiles(f"decode_split_kernel<64,128> {wd.name}",
-                                                     os.path.join(csrc, "decode_sm103a.cuh"))}
+                    "traffic": traffic_from_profiles("decode_split_kernel<64,128>", wd.name)}
         line["decode"] = {"value": dec_gbs, "unit": "GB/s", "ms": dec_ms / args.steps, "roofline": dec_roof}
     if do_pre:
         pre_tflops = wp.flops * args.steps * world / (pre_ms * 1e-3) / 1e12
@@ -590,8 +594,7 @@ def run_cuda(args, world, rank, local):
         line["roofline"] = {"bound": "tensor", "achieved": pre_tflops / world, "peak": peak_b, "unit": "TFLOP/s",
                             "frac": pre_tflops / world / peak_b, "peak_source": f"{peak_src} burst",
                             "frac_of_sustained": pre_tflops / world / peak_s,
-                            "traffic": traffic_from_profiles(f"prefill_kernel<64,128,causal> {wp.name}",
-                                                             os.path.join(csrc, "prefill_sm103a.cuh"))}
+                            "traffic": traffic_from_profiles("prefill_kernel<64,128,causal>", wp.name)}
     else:
         line["value"], line["unit"] = line["decode"]["value"], "GB/s"
         line["roofline"] = line["decode"]["roofline"]

@@ -29,12 +29,21 @@ def test_reference_arm_prints_one_contract_line():
 
 
 def test_traffic_table_is_used_only_for_the_profiled_source(tmp_path):
-    src = os.path.join(ROOT, "transformer_attention_07_b300", "csrc", "prefill_sm103a.cuh")
-    key = "prefill_kernel<64,128,causal> long_64k"
-    t = bench.traffic_from_profiles(key, src)
-    # The committed table was taken on the committed kernel source.
-    assert isinstance(t, int) and t > 0
-    changed = tmp_path / "prefill_sm103a.cuh"
+    table = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    for e in table["entries"]:
+        # every record names an existing source file and a whole byte count
+        assert os.path.exists(os.path.join(ROOT, e["source"]))
+        assert isinstance(e["bytes_per_launch"], int) and e["bytes_per_launch"] > 0
+        assert e["command"].count("ncu") >= 1 and "--clock-control none" in e["command"]
+    e = table["entries"][0]
+    src = os.path.join(ROOT, e["source"])
+    # The same record against a changed copy of its source is not used.
+    changed = tmp_path / "changed.cuh"
     changed.write_bytes(open(src, "rb").read() + b"\n// changed\n")
-    assert bench.traffic_from_profiles(key, str(changed)) is None
-    assert bench.traffic_from_profiles("no such kernel", src) is None
+    same = tmp_path / "same.cuh"
+    same.write_bytes(open(src, "rb").read())
+    for path, expect in ((same, e["bytes_per_launch"]), (changed, None)):
+        t = tmp_path / "t.json"
+        t.write_text(json.dumps({"entries": [dict(e, source=str(path))]}))
+        assert bench.traffic_from_profiles(e["kernel"], e["workload"], str(t)) == expect
+    assert bench.traffic_from_profiles("no such kernel", e["workload"]) is None

@@ -99,16 +99,22 @@ def test_decode_repeated_runs_agree_bitwise(splits):
     assert np.abs(pre_s - o_ref).max() <= TOL_PRE
 
 
-def test_decode_32k_sampled_heads():
-    """Full-size decode (B=32, H=32, Nk=32768): the whole batch runs on the
-    GPU; 24 seeded (b, h) heads are checked against the oracle."""
+def test_decode_32k_every_head():
+    """Full-size decode (B=32, H=32, Nk=32768), every (b, h) against the
+    oracle: the GPU runs the whole batch once; the caches are then copied to
+    the host one batch entry (512 MiB) at a time and the oracle computes that
+    entry's 32 heads over all 32768 keys."""
     w = WORKLOADS["decode_32k"]
     inp = make_inputs(w)
     out, pre = gpu_decode(inp, w.lam, w.lam_init, eps=w.eps)
-    g = torch.Generator().manual_seed(w.seed)
-    heads = torch.randperm(w.B * w.H, generator=g)[:24].tolist()
-    sel = {k: torch.stack([inp[k][h // w.H, h % w.H] for h in heads])[:, None] for k in ("q1", "k1", "q2", "k2", "v")}
-    o_ref, y_ref = oracle_decode(sel, w.lam, w.lam_init, w.eps)
-    out_s = torch.stack([out[h // w.H, h % w.H] for h in heads])[:, None]
-    pre_s = torch.stack([pre[h // w.H, h % w.H] for h in heads])[:, None]
-    check(out_s, pre_s, o_ref, y_ref)
+    worst_pre = worst_out = 0.0
+    for b in range(w.B):
+        sel = {k: inp[k][b:b + 1] for k in ("q1", "k1", "q2", "k2", "v")}
+        o_ref, y_ref = oracle_decode(sel, w.lam, w.lam_init, w.eps)
+        got_pre = pre[b:b + 1].cpu().numpy()
+        got_out = out[b:b + 1].float().cpu().numpy()
+        assert np.isfinite(got_pre).all() and np.isfinite(got_out).all()
+        worst_pre = max(worst_pre, float(np.abs(got_pre - o_ref).max()))
+        worst_out = max(worst_out, float(np.abs(got_out - y_ref).max()))
+    print(f"[parity] decode_32k, all {w.B * w.H} heads: pre-norm {worst_pre:.3e}, normalised {worst_out:.3e}")
+    assert worst_pre <= TOL_PRE and worst_out <= TOL_OUT

@@ -91,3 +91,56 @@ def test_gather_partials_stacks_ranks_in_order():
         assert tuple(shape) == (2, 3, 2, 2, 8)
         assert firsts == [0.0, 1.0]
         assert own
+
+
+def test_head_range_partitions_every_head_once():
+    """The head-partitioned prefill's split of B*H heads over the ranks:
+    contiguous, in rank order, sizes within one of each other."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import transformer_attention_07_b300 as da
+    for heads in (0, 1, 5, 16, 17, 1024):
+        for world in (1, 2, 3, 8):
+            ranges = [da.head_range(heads, world, r) for r in range(world)]
+            assert ranges[0][0] == 0 and ranges[-1][1] == heads
+            assert all(ranges[r][1] == ranges[r + 1][0] for r in range(world - 1))
+            sizes = [hi - lo for lo, hi in ranges]
+            assert max(sizes) - min(sizes) <= 1
+    with pytest.raises(ValueError):
+        da.head_range(4, 2, 2)
+
+
+def _heads_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import transformer_attention_07_b300 as da
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        B, H = 3, 5   # 15 heads over the ranks: unequal shares
+        lo, hi = da.head_range(B * H, world, rank)
+        # this rank's output slice: head i holds the value i everywhere
+        mine = torch.arange(lo, hi, dtype=torch.float32).view(-1, 1, 1).expand(hi - lo, 4, 6).contiguous()
+        full = da.gather_heads(mine, B, H)
+        q.put((rank, tuple(full.shape), full[:, 0, 0].tolist()))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_gather_heads_reassembles_the_output_in_head_order(world):
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_heads_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    results = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for _, shape, firsts in results:
+        assert shape == (15, 4, 6)
+        assert firsts == [float(i) for i in range(15)]

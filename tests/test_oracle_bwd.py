@@ -166,3 +166,29 @@ def test_bwd_rejects_bad_arguments():
         oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy[:, :, :3], 0.5, 0.8)
     with pytest.raises(ValueError):
         oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, 0.5, 0.8, rows=[4])
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,causal,lam", [
+    (2, 2, 64, 64, True, 0.5), (1, 2, 40, 70, False, -0.3), (2, 1, 30, 20, False, 0.0), (1, 3, 50, 90, True, 0.8)])
+def test_dlambda_bound_rejects_plausible_kernel_mistakes(B, H, Nq, Nk, causal, lam):
+    """The GPU tests accept dlambda within 1e-2 |dlambda| + 3.2e-3 rss (rss =
+    root-sum-square of the per-row terms; tests/dlambda_bound.py derives it
+    from the forward's bf16 rounding).  On oracle gradients of problems like
+    the GPU tests' (no GPU needed), that bound must reject what a kernel
+    mistake would produce: the lambda term's sign flipped (-dlambda), the
+    term dropped (0), or the terms of half the rows left out."""
+    from dlambda_bound import assert_rejects_plausible_bugs, bound
+    t, dy, gamma = problem(B, H, Nq, Nk, 64, 128, seed=B * 1000 + Nq + Nk)
+    g = oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy, lam, 0.8, causal=causal, gamma=gamma)
+    ref, rss = g["dlambda"], g["dlambda_rss"]
+    assert_rejects_plausible_bugs(ref, rss)
+    b = bound(ref, rss)
+    for wrong in (-ref, 0.0):
+        assert abs(wrong - ref) > b
+    # Every second row's term dropped (a kernel summing only part of the
+    # rows): the oracle's dlambda of the loss restricted to the other rows.
+    dy_half = dy.copy()
+    dy_half[:, :, 1::2] = 0.0
+    part = oracle.diffattn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], dy_half, lam, 0.8, causal=causal,
+                               gamma=gamma)["dlambda"]
+    assert abs(part - ref) > b

@@ -20,8 +20,8 @@ import os
 __all__ = [
     "fwd", "fwd_host", "fwd_host_workspace_bytes", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes",
     "standard_fwd", "decode", "decode_paged", "decode_workspace_bytes", "decode_partials", "decode_partials_bytes",
-    "decode_merge", "gather_partials", "decode_sharded", "status_string", "last_device_error",
-    "selftest_wait_timeout", "load", "LIB_PATH",
+    "decode_merge", "gather_partials", "decode_sharded", "head_range", "gather_heads", "fwd_sharded",
+    "status_string", "last_device_error", "selftest_wait_timeout", "load", "LIB_PATH",
     "DiffAttnError", "SUPPORTED_WIDTHS",
 ]
 
@@ -400,16 +400,81 @@ def decode_merge(partials, B, H, lam, lam_init, gamma=None, eps=1e-5, out=None, 
     return out
 
 
+def _all_gather(t, group):
+    """All-gather ``t`` over ``group``: [world, *t.shape] in rank order, on
+    t's device.  A gloo group exchanges host copies (gloo moves host memory);
+    NCCL exchanges the device tensors directly."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size(group)
+    src = t.contiguous()
+    if src.is_cuda and dist.get_backend(group) == "gloo":
+        src = src.cpu()
+    chunks = [torch.empty_like(src) for _ in range(world)]
+    dist.all_gather(chunks, src, group=group)
+    return torch.stack(chunks).to(t.device)
+
+
 def gather_partials(partials, group=None):
     """All-gather the partial states of every rank of ``group`` (torch.distributed):
     returns [world, *partials.shape], rank order, the layout decode_merge reads.
     This is the one exchange step of sequence-sharded decode."""
+    return _all_gather(partials, group)
+
+
+def head_range(heads, world, rank):
+    """The contiguous range [lo, hi) of flattened (b, h) heads that ``rank``
+    of ``world`` computes in a head-partitioned prefill: sizes differ by at
+    most one, every head belongs to exactly one rank, in rank order."""
+    if world < 1 or not 0 <= rank < world or heads < 0:
+        raise ValueError("need world >= 1, 0 <= rank < world and heads >= 0")
+    return rank * heads // world, (rank + 1) * heads // world
+
+
+def fwd_sharded(q1, k1, q2, k2, v, lam, lam_init, causal=False, gamma=None, eps=1e-5, group=None, gather=False,
+                stream=None):
+    """Prefill with the B*H independent heads partitioned over the ranks of
+    ``group``: every rank passes the full inputs (or at least its heads) and
+    computes the heads ``head_range(B*H, world, rank)`` of the flattened
+    [B*H, N, width] view, with no exchange.  Returns this rank's slice of
+    ``out`` as [hi - lo, Nq, dv]; with ``gather=True`` the slices of every
+    rank are all-gathered into the full [B, H, Nq, dv] output on every rank
+    (the only collective, needed only when one GPU consumes all heads)."""
+    import torch
+    import torch.distributed as dist
+    B, H, Nq, _ = q1.shape
+    dv = v.shape[3]
+    world, rank = dist.get_world_size(group), dist.get_rank(group)
+    lo, hi = head_range(B * H, world, rank)
+    view = lambda t: t.reshape(1, B * H, t.shape[2], t.shape[3])[:, lo:hi]
+    # Each flattened head keeps its own gain slice: gamma [H*dv] repeated over B.
+    g = None if gamma is None else gamma.view(1, H * dv).expand(B, H * dv).reshape(B * H, dv)[lo:hi].reshape(-1)
+    out = torch.empty((1, hi - lo, Nq, dv), dtype=torch.bfloat16, device=q1.device)
+    if hi > lo:
+        fwd(*(view(t).contiguous() for t in (q1, k1, q2, k2, v)), lam, lam_init, causal=causal,
+            gamma=None if g is None else g.contiguous(), eps=eps, out=out, stream=stream)
+    if not gather:
+        return out[0]
+    if stream is not None:
+        torch.cuda.current_stream(q1.device).wait_stream(stream)
+    return gather_heads(out[0], B, H, group).view(B, H, Nq, dv)
+
+
+def gather_heads(mine, B, H, group=None):
+    """All-gather the head slices of a head-partitioned prefill: ``mine`` is
+    this rank's [hi - lo, ...] slice (``head_range``); returns the full
+    [B*H, ...] tensor on every rank, heads in order.  Slices are padded to the
+    largest share for the exchange and the padding is dropped after it."""
     import torch
     import torch.distributed as dist
     world = dist.get_world_size(group)
-    chunks = [torch.empty_like(partials) for _ in range(world)]
-    dist.all_gather(chunks, partials.contiguous(), group=group)
-    return torch.stack(chunks)
+    sizes = [hi - lo for lo, hi in (head_range(B * H, world, r) for r in range(world))]
+    if mine.shape[0] != sizes[dist.get_rank(group)]:
+        raise ValueError("mine must hold exactly this rank's heads")
+    pad = torch.zeros((max(sizes),) + tuple(mine.shape[1:]), dtype=mine.dtype, device=mine.device)
+    pad[: mine.shape[0]].copy_(mine)
+    every = _all_gather(pad, group)
+    return torch.cat([every[r, : sizes[r]] for r in range(world)])
 
 
 def decode_sharded(q1, k1, q2, k2, v, lam, lam_init, num_splits=8, gamma=None, eps=1e-5, group=None, stream=None):

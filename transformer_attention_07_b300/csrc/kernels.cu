@@ -148,11 +148,12 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     const int sms = sm_count();
     const bool persist = sms > 0 && tiles > sms && a.Nk <= kPersistMaxNk;
     auto kern = persist ? prefill_kernel<D, DV, CAUSAL, QK8, true> : prefill_kernel<D, DV, CAUSAL, QK8, false>;
-    if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
+    const int smem = (int)(persist ? PrefillLayout<D, DV, QK8, true>::SMEM_BYTES : L::SMEM_BYTES);
+    if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
                  "prefill: set shared memory"))
         return LAUNCH_ERR_CUDA;
     const dim3 grid = persist ? dim3(sms, 1, 1) : dim3((a.Nq + L::BM - 1) / L::BM, a.H, a.B);
-    kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq1, mq2, mk1, mk2, mv, p);
+    kern<<<grid, L::THREADS, smem, st>>>(mq1, mq2, mk1, mk2, mv, p);
     return cuda_ok(cudaGetLastError(), "prefill: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }
 

@@ -58,12 +58,19 @@ struct PrefillParams {
 // QK8: Q1, Q2, K1, K2 are fp8 (e4m3) with per-head scales, and Q K^T runs
 // as an 8-bit tensor-core product (kind::f8f6f4, K = 32 per instruction);
 // P V stays bf16.
-template <int D, int DV, bool QK8 = false>
+// PERSIST: the layout of the persistent form (see prefill_kernel).
+template <int D, int DV, bool QK8 = false, bool PERSIST = false>
 struct PrefillLayout {
     static constexpr int BM = 128;   // query rows per tile (MMA M)
     static constexpr int BN = 128;   // keys per tile (MMA N of QK^T, K of PV)
     static constexpr int KST = 3;    // K1/K2 ring depth
-    static constexpr int VST = 2;    // V ring depth
+    // V ring depth.  A V tile can be loaded only once the P V product two
+    // (three) tiles back has completed, and from L2 under full load it takes
+    // about as long as one key tile's work to arrive, so a third stage keeps
+    // the tensor core from waiting on it.  The persistent form needs its own
+    // epilogue slots (the next tile's loads run during the epilogue) and has
+    // no room for it.
+    static constexpr int VST = PERSIST ? 2 : 3;
     static constexpr uint32_t QK_ELEM = QK8 ? 1 : 2;   // bytes per Q/K element
     static constexpr uint32_t QK_ROW = D * QK_ELEM;    // bytes per Q/K row: 128, 64 or 32
     static constexpr uint32_t Q_BYTES = BM * QK_ROW;
@@ -74,8 +81,12 @@ struct PrefillLayout {
     static constexpr uint32_t OFF_Q2 = Q_BYTES;
     static constexpr uint32_t OFF_K = 2 * Q_BYTES;              // stage s: K1 then K2
     static constexpr uint32_t OFF_V = OFF_K + KST * 2 * K_BYTES;
-    static constexpr uint32_t OFF_EPI = OFF_V + VST * V_BYTES;  // 6 x 128 fp32 exchange slots
-    static constexpr uint32_t OFF_BAR = OFF_EPI + 6 * BM * 4;
+    // 6 x 128 fp32 exchange slots of the epilogue.  With one query tile per
+    // CTA they lie over Q1, which nothing reads once the epilogue may start.
+    static constexpr uint32_t EPI_BYTES = 6 * BM * 4;
+    static_assert(EPI_BYTES <= Q_BYTES, "epilogue slots");
+    static constexpr uint32_t OFF_EPI = PERSIST ? OFF_V + VST * V_BYTES : OFF_Q1;
+    static constexpr uint32_t OFF_BAR = PERSIST ? OFF_EPI + EPI_BYTES : OFF_V + VST * V_BYTES;
     // barrier indices
     static constexpr int B_Q = 0;
     static constexpr int B_KFULL = 1;
@@ -111,7 +122,7 @@ __global__ void __launch_bounds__(384, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
                const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
                const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-    using L = PrefillLayout<D, DV, QK8>;
+    using L = PrefillLayout<D, DV, QK8, PERSIST>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_addr(smem);
@@ -238,14 +249,20 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop with warp-uniform values; each MMA and
+        // commit is issued by one elected lane (the *_warp wrappers).
+        {
             constexpr uint32_t idesc_qk = QK8 ? idesc_e4m3_f32(L::BM, L::BN) : idesc_bf16_f32(L::BM, L::BN, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(L::BM, DV, true);
-            bool ok = mbar_wait(bar(L::B_Q), 0, ERR_SITE_PREFILL_MMA);
+            // Every lane waits; a wait that ran out on any lane ends the loop on all.
+            auto wait = [&](int i, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ERR_SITE_PREFILL_MMA));
+            };
+            bool ok = wait(L::B_Q, 0);
             tc_fence_after();
             // Operand descriptors are built once; stages and k-steps are
             // compile-time offsets in the descriptor's address field (units of
-            // 16 bytes), so each MMA costs one add: the issuing thread's own
+            // 16 bytes), so each MMA costs one add: the issuing warp's own
             // instruction latency otherwise bounds the tensor pipe.
             const uint64_t dq1 = smem_desc(sb + L::OFF_Q1, 16, L::QK_SBO, L::QK_SWZ);
             const uint64_t dq2 = smem_desc(sb + L::OFF_Q2, 16, L::QK_SBO, L::QK_SWZ);
@@ -258,16 +275,18 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             auto pv = [&](uint32_t t_o, uint32_t t_p, uint64_t dvs, uint32_t acc0) {
 #pragma unroll
                 for (int k = 0; k < L::BN / 16; ++k)
-                    mma_ts(t_o, t_p + 8u * k, dvs + (uint64_t)(k * (16 * 128 >> 4)), idesc_pv, k == 0 ? acc0 : 1u);
+                    mma_ts_warp(t_o, t_p + 8u * k, dvs + (uint64_t)(k * (16 * 128 >> 4)), idesc_pv,
+                                k == 0 ? acc0 : 1u);
             };
             // S = Q K^T over one key tile: 16-column steps of d (32 bytes).
             auto qk = [&](uint32_t t_s, uint64_t dq, uint64_t dks) {
 #pragma unroll
                 for (int k = 0; k < L::QK_KSTEPS; ++k) {
                     if constexpr (QK8)
-                        mma_ss_f8(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk, k > 0 ? 1u : 0u);
+                        mma_ss_f8_warp(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk,
+                                       k > 0 ? 1u : 0u);
                     else
-                        mma_ss(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk, k > 0 ? 1u : 0u);
+                        mma_ss_warp(t_s, dq + (uint64_t)(2 * k), dks + (uint64_t)(2 * k), idesc_qk, k > 0 ? 1u : 0u);
                 }
             };
             int g = 0;   // key tiles of earlier query tiles (ring stage and phase counter)
@@ -275,70 +294,67 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             for (int k = 0; ok && tile(k, qt, h, b); ++k) {
                 const int n_kv = kv_tiles(qt);
                 if (k > 0) {
-                    ok = mbar_wait(bar(L::B_Q), k & 1, ERR_SITE_PREFILL_MMA);
+                    ok = wait(L::B_Q, k & 1);
                     if (!ok) break;
                     tc_fence_after();
                 }
+                // Step j: P V of key tile j - 1, then the scores of tile j, per
+                // map.  P_r V waits only for V and P_r, the scores only for K,
+                // so a late K tile does not hold up the P V products.
                 for (int j = 0; j <= n_kv; ++j) {
                     const int gj = g + j;
                     const int ks = gj % L::KST;
-                    if (j < n_kv) {
-                        ok = mbar_wait(bar(L::B_KFULL + ks), (gj / L::KST) & 1, ERR_SITE_PREFILL_MMA);
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
                     const int jv = j - 1, gv = gj - 1;
                     const int vs = (gv + L::VST) % L::VST;
-                    if (jv >= 0) {
-                        ok = mbar_wait(bar(L::B_VFULL + vs), (gv / L::VST) & 1, ERR_SITE_PREFILL_MMA);
-                        if (!ok) break;
-                    }
                     const uint64_t dvs = dv0 + (uint64_t)vs * VSTAGE;
                     const uint64_t dks = dk0 + (uint64_t)ks * KSTAGE;
                     const uint32_t acc0 = jv > 0 ? 1u : 0u;
                     // map 1: O1 += P1 V (previous tile), then S1 = Q1 K1^T (this tile)
                     if (jv >= 0) {
-                        ok = mbar_wait(bar(L::B_PFULL + 0), gv & 1, ERR_SITE_PREFILL_MMA);
+                        ok = wait(L::B_VFULL + vs, (gv / L::VST) & 1) && wait(L::B_PFULL + 0, gv & 1);
                         if (!ok) break;
                         if (PERSIST && jv == 0 && k > 0) {
                             // The first product of a query tile overwrites O:
                             // the previous tile's epilogue must have read it.
-                            ok = mbar_wait(bar(L::B_OFREE), (k - 1) & 1, ERR_SITE_PREFILL_MMA);
+                            ok = wait(L::B_OFREE, (k - 1) & 1);
                             if (!ok) break;
                         }
                         tc_fence_after();
                         pv(t_o1, t_s1, dvs, acc0);
                     }
                     if (j < n_kv) {
+                        ok = wait(L::B_KFULL + ks, (gj / L::KST) & 1);
+                        if (!ok) break;
+                        tc_fence_after();
                         qk(t_s1, dq1, dks);
-                        mma_commit(bar(L::B_SFULL + 0));
+                        mma_commit_warp(bar(L::B_SFULL + 0));
                     }
                     // map 2
                     if (jv >= 0) {
-                        ok = mbar_wait(bar(L::B_PFULL + 1), gv & 1, ERR_SITE_PREFILL_MMA);
+                        ok = wait(L::B_PFULL + 1, gv & 1);
                         if (!ok) break;
                         tc_fence_after();
                         pv(t_o2, t_s2, dvs, acc0);
-                        mma_commit(bar(L::B_VEMPTY + vs));
+                        mma_commit_warp(bar(L::B_VEMPTY + vs));
                     }
                     if (j < n_kv) {
                         qk(t_s2, dq2, dks + K2_OFF);
-                        mma_commit(bar(L::B_SFULL + 1));
-                        mma_commit(bar(L::B_KEMPTY + ks));
-                        if (PERSIST && j == n_kv - 1) mma_commit(bar(L::B_QEMPTY));
+                        mma_commit_warp(bar(L::B_SFULL + 1));
+                        mma_commit_warp(bar(L::B_KEMPTY + ks));
+                        if (PERSIST && j == n_kv - 1) mma_commit_warp(bar(L::B_QEMPTY));
                     }
                 }
                 g += n_kv;
                 // The epilogue of this query tile may start once every MMA
                 // issued so far has completed.
-                if (ok) mma_commit(bar(L::B_OFULL));
+                if (ok) mma_commit_warp(bar(L::B_OFULL));
                 if constexpr (!PERSIST) break;
             }
             if (!ok) {
                 // Error: signal the epilogue anyway, and let no MMA outlive
                 // the kernel's tensor memory.
-                mma_commit(bar(L::B_OFULL));
-                mma_commit(bar(L::B_DRAIN));
+                mma_commit_warp(bar(L::B_OFULL));
+                mma_commit_warp(bar(L::B_DRAIN));
                 mbar_wait(bar(L::B_DRAIN), 0, ERR_SITE_PREFILL_DRAIN);
             }
         }

@@ -398,10 +398,16 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop with warp-uniform values; each MMA and
+        // commit is issued by one elected lane (the *_warp wrappers).
+        {
+            // Every lane waits; a wait that ran out on any lane ends the loop on all.
+            auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, ERR_SITE_BWD_MMA));
+            };
             constexpr uint32_t idesc_s = idesc_bf16_f32(L::BM, L::BN, false);   // S, dP: K-major operands
             constexpr uint32_t idesc_dq = idesc_bf16_f32(L::BM, D, true);       // dQ: K tile MN-major
-            bool ok = mbar_wait(bar(L::B_Q), 0, ERR_SITE_BWD_MMA);
+            bool ok = wait(bar(L::B_Q), 0);
             tc_fence_after();
             const uint64_t dq1 = smem_desc(sb + L::OFF_Q1, 16, L::QK_SBO, L::QK_SWZ);
             const uint64_t dq2 = smem_desc(sb + L::OFF_Q2, 16, L::QK_SBO, L::QK_SWZ);
@@ -414,7 +420,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             auto dp_mma = [&](uint64_t so) {
 #pragma unroll
                 for (int k = 0; k < DV / 16; ++k)
-                    mma_ss(tmem + L::TM_DP, ddo + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4),
+                    mma_ss_warp(tmem + L::TM_DP, ddo + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4),
                            dv0 + so + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4), idesc_s,
                            k > 0 ? 1u : 0u);
             };
@@ -422,7 +428,7 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             auto s_mma = [&](int r, uint64_t so) {
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    mma_ss(tmem + (r ? L::TM_S2 : L::TM_S1), (r ? dq2 : dq1) + (uint64_t)(2 * k),
+                    mma_ss_warp(tmem + (r ? L::TM_S2 : L::TM_S1), (r ? dq2 : dq1) + (uint64_t)(2 * k),
                            dk0 + so + (r ? K2OFF : 0) + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
             };
             // dQ_r += dS_r K_r: dS_r (bf16) in the first 64 columns of S_r,
@@ -430,20 +436,20 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             auto dq_mma = [&](int r, uint64_t so, bool first) {
 #pragma unroll
                 for (int k = 0; k < L::BN / 16; ++k)
-                    mma_ts(tmem + (r ? L::TM_DQ2 : L::TM_DQ1), tmem + (r ? L::TM_S2 : L::TM_S1) + 8u * k,
+                    mma_ts_warp(tmem + (r ? L::TM_DQ2 : L::TM_DQ1), tmem + (r ? L::TM_S2 : L::TM_S1) + 8u * k,
                            dkm0 + so + (r ? K2OFF : 0) + (uint64_t)(k * (16 * L::QK_ROW >> 4)), idesc_dq,
                            (!first || k > 0) ? 1u : 0u);
             };
-            if (ok) ok = mbar_wait(bar(L::B_VFULL + 0), 0, ERR_SITE_BWD_MMA);
-            if (ok) ok = mbar_wait(bar(L::B_KFULL + 0), 0, ERR_SITE_BWD_MMA);
+            if (ok) ok = wait(bar(L::B_VFULL + 0), 0);
+            if (ok) ok = wait(bar(L::B_KFULL + 0), 0);
             if (ok) {
                 tc_fence_after();
                 dp_mma(0);
-                mma_commit(bar(L::B_VEMPTY + 0));
+                mma_commit_warp(bar(L::B_VEMPTY + 0));
                 s_mma(0, 0);
-                mma_commit(bar(L::B_SFULL + 0));
+                mma_commit_warp(bar(L::B_SFULL + 0));
                 s_mma(1, 0);
-                mma_commit(bar(L::B_SFULL + 1));
+                mma_commit_warp(bar(L::B_SFULL + 1));
             }
             // Per tile j: map 1's dQ product, its next scores, then the next
             // dP (once both maps hold this tile's dP), which completes the
@@ -454,35 +460,35 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
                 const uint64_t so = (uint64_t)(j % L::KST) * KSTAGE16;
                 const bool more = j + 1 < n_kv;
                 const uint64_t sn = (uint64_t)((j + 1) % L::KST) * KSTAGE16;
-                ok = mbar_wait(bar(L::B_PFULL + 0), j & 1, ERR_SITE_BWD_MMA);
+                ok = wait(bar(L::B_PFULL + 0), j & 1);
                 if (!ok) break;
                 tc_fence_after();
                 dq_mma(0, so, j == 0);
                 if (more) {
-                    ok = mbar_wait(bar(L::B_KFULL + (j + 1) % L::KST), ((j + 1) / L::KST) & 1, ERR_SITE_BWD_MMA);
+                    ok = wait(bar(L::B_KFULL + (j + 1) % L::KST), ((j + 1) / L::KST) & 1);
                     if (!ok) break;
                     tc_fence_after();
                     s_mma(0, sn);
                     const int vs = (j + 1) % L::VST;
-                    ok = mbar_wait(bar(L::B_VFULL + vs), ((j + 1) / L::VST) & 1, ERR_SITE_BWD_MMA);
-                    ok = ok && mbar_wait(bar(L::B_DPFREE), j & 1, ERR_SITE_BWD_MMA);
+                    ok = wait(bar(L::B_VFULL + vs), ((j + 1) / L::VST) & 1);
+                    ok = ok && wait(bar(L::B_DPFREE), j & 1);
                     if (!ok) break;
                     tc_fence_after();
                     dp_mma((uint64_t)vs * VSTAGE16);
-                    mma_commit(bar(L::B_VEMPTY + vs));
-                    mma_commit(bar(L::B_SFULL + 0));
+                    mma_commit_warp(bar(L::B_VEMPTY + vs));
+                    mma_commit_warp(bar(L::B_SFULL + 0));
                 }
-                ok = mbar_wait(bar(L::B_PFULL + 1), j & 1, ERR_SITE_BWD_MMA);
+                ok = wait(bar(L::B_PFULL + 1), j & 1);
                 if (!ok) break;
                 tc_fence_after();
                 dq_mma(1, so, j == 0);
-                mma_commit(bar(L::B_KEMPTY + j % L::KST));
+                mma_commit_warp(bar(L::B_KEMPTY + j % L::KST));
                 if (more) {
                     s_mma(1, sn);
-                    mma_commit(bar(L::B_SFULL + 1));
+                    mma_commit_warp(bar(L::B_SFULL + 1));
                 }
             }
-            mma_commit(bar(L::B_DQFULL));
+            mma_commit_warp(bar(L::B_DQFULL));
         }
         __syncwarp();
     } else {
@@ -728,11 +734,17 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop with warp-uniform values; each MMA and
+        // commit is issued by one elected lane (the *_warp wrappers).
+        {
+            // Every lane waits; a wait that ran out on any lane ends the loop on all.
+            auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(b, parity, ERR_SITE_BWD_MMA));
+            };
             constexpr uint32_t idesc_s = idesc_bf16_f32(L::BK, L::BQ, false);   // S^T, dP^T
             constexpr uint32_t idesc_dv = idesc_bf16_f32(L::BK, DV, true);      // dV: dO MN-major
             constexpr uint32_t idesc_dk = idesc_bf16_f32(L::BK, D, true);       // dK: Q MN-major
-            bool ok = mbar_wait(bar(L::B_KV), 0, ERR_SITE_BWD_MMA);
+            bool ok = wait(bar(L::B_KV), 0);
             tc_fence_after();
             const uint64_t dk1 = smem_desc(sb + L::OFF_K1, 16, L::QK_SBO, L::QK_SWZ);
             const uint64_t dk2 = smem_desc(sb + L::OFF_K2, 16, L::QK_SBO, L::QK_SWZ);
@@ -750,15 +762,15 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             // is released.
             auto issue_scores = [&](int t) -> bool {
                 const uint64_t st = (uint64_t)(t % L::QST) * STAGE16;
-                if (!mbar_wait(bar(L::B_QFULL + t % L::QST), (t / L::QST) & 1, ERR_SITE_BWD_MMA)) return false;
+                if (!wait(bar(L::B_QFULL + t % L::QST), (t / L::QST) & 1)) return false;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    mma_ss(ta, dk1 + (uint64_t)(2 * k), dq0 + st + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
-                mma_commit(bar(L::B_S1FULL));
+                    mma_ss_warp(ta, dk1 + (uint64_t)(2 * k), dq0 + st + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
+                mma_commit_warp(bar(L::B_S1FULL));
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    mma_ss(tb, dk2 + (uint64_t)(2 * k), dq0 + st + Q2OFF + (uint64_t)(2 * k), idesc_s,
+                    mma_ss_warp(tb, dk2 + (uint64_t)(2 * k), dq0 + st + Q2OFF + (uint64_t)(2 * k), idesc_s,
                            k > 0 ? 1u : 0u);
                 return true;
             };
@@ -768,15 +780,15 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 const uint64_t st = (uint64_t)qs * STAGE16;
                 // dP^T = V dO^T over S1^T once the dS warps hold it: k over
                 // dv, two 64-column boxes of each operand.
-                ok = mbar_wait(bar(L::B_S1FREE), t & 1, ERR_SITE_BWD_MMA);
+                ok = wait(bar(L::B_S1FREE), t & 1);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < DV / 16; ++k)
-                    mma_ss(ta, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
+                    mma_ss_warp(ta, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
                            ddo0 + st + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
                            k > 0 ? 1u : 0u);
-                mma_commit(bar(L::B_DPFULL));
+                mma_commit_warp(bar(L::B_DPFULL));
                 // Gradients, chunk by chunk: chunk c is queries
                 // [64 hh + CW c, 64 hh + CW c + CW) of each half hh, CW / 16
                 // k-steps; in bf16 its dS1^T, dS2^T fill the chunk's columns
@@ -784,7 +796,7 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 // (A1 - lambda A2)^T the first CW / 2 of region B.
 #pragma unroll
                 for (int c = 0; c < L::NCH; ++c) {
-                    ok = mbar_wait(bar(L::B_PFULL + c), t & 1, ERR_SITE_BWD_MMA);
+                    ok = wait(bar(L::B_PFULL + c), t & 1);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
@@ -796,9 +808,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                                            kq = (uint64_t)(k * (16 * L::QK_ROW >> 4));
                             const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
                             const uint32_t col = 64u * hh + L::CW * c + 8u * sub;
-                            mma_ts(tmem + L::TM_DV, tb + col, ddom0 + st + kd, idesc_dv, acc);
-                            mma_ts(tmem + L::TM_DK1, ta + col, dqm0 + st + kq, idesc_dk, acc);
-                            mma_ts(tmem + L::TM_DK2, ta + col + L::CW / 2, dqm0 + st + Q2OFF + kq, idesc_dk, acc);
+                            mma_ts_warp(tmem + L::TM_DV, tb + col, ddom0 + st + kd, idesc_dv, acc);
+                            mma_ts_warp(tmem + L::TM_DK1, ta + col, dqm0 + st + kq, idesc_dk, acc);
+                            mma_ts_warp(tmem + L::TM_DK2, ta + col + L::CW / 2, dqm0 + st + Q2OFF + kq, idesc_dk, acc);
                         }
                     }
                 }
@@ -807,9 +819,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                     ok = issue_scores(t + 1);
                     if (!ok) break;
                 }
-                mma_commit(bar(L::B_QEMPTY + qs));
+                mma_commit_warp(bar(L::B_QEMPTY + qs));
             }
-            mma_commit(bar(L::B_DONE));
+            mma_commit_warp(bar(L::B_DONE));
         }
         __syncwarp();
     } else {

@@ -17,7 +17,8 @@
 // (PERSIST) walks such tile pairs with one CTA per SM for short sequences.
 // Warp roles:
 //   warp 0       TMA producer: both Q tiles once, then K and V tiles.
-//   warp 1       tensor-core issuer: per key tile and query tile r,
+//   warp 1       tensor-core issuer (the whole warp; one elected lane
+//                issues): per key tile and query tile r,
 //                O_r += P_r V (previous key tile, A = P in TMEM) then
 //                S_r = Q_r K^T (A and B in smem, K-dim 128 = two 64-column
 //                swizzle atoms).
@@ -204,10 +205,16 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        // The whole warp runs this loop with warp-uniform values; each MMA and
+        // commit is issued by one elected lane (the *_warp wrappers).
+        {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(L::BM, L::BN, false);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(L::BM, L::DV, true);
-            bool ok = mbar_wait(bar(L::B_Q), 0, ERR_SITE_PREFILL_MMA);
+            // Every lane waits; a wait that ran out on any lane ends the loop on all.
+            auto wait = [&](int i, uint32_t parity) -> bool {
+                return __all_sync(0xffffffffu, mbar_wait(bar(i), parity, ERR_SITE_PREFILL_MMA));
+            };
+            bool ok = wait(L::B_Q, 0);
             tc_fence_after();
             const uint32_t s_col[2] = {L::TM_S0, L::TM_S1};
             const uint32_t o_col[2] = {L::TM_O0, L::TM_O1};
@@ -216,69 +223,67 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             for (int k = 0; ok && tile(k, pr, h, b); ++k) {
             const int n_kv = kv_tiles(pr);
             if (k > 0) {
-                ok = mbar_wait(bar(L::B_Q), k & 1, ERR_SITE_PREFILL_MMA);
+                ok = wait(L::B_Q, k & 1);
                 if (!ok) break;
                 tc_fence_after();
             }
+            // Step j: P V of key tile j - 1, then the scores of tile j, per
+            // query tile.  P V waits only for V and P, the scores only for K.
             for (int j = 0; j <= n_kv && ok; ++j) {
                 const int gj = g + j;
                 const int ks = gj % L::KST;
-                if (j < n_kv) {
-                    ok = mbar_wait(bar(L::B_KFULL + ks), (gj / L::KST) & 1, ERR_SITE_PREFILL_MMA);
-                    if (!ok) break;
-                    tc_fence_after();
-                }
                 const int jv = j - 1, gv = gj - 1;
                 const int vs = (gv + L::VST) % L::VST;
-                if (jv >= 0) {
-                    ok = mbar_wait(bar(L::B_VFULL + vs), (gv / L::VST) & 1, ERR_SITE_PREFILL_MMA);
-                    if (!ok) break;
-                }
                 const uint32_t vsm = sb + L::OFF_V + (uint32_t)vs * L::V_BYTES;
                 const uint32_t kst = sb + L::OFF_K + (uint32_t)ks * L::K_BYTES;
                 for (int r = 0; r < 2; ++r) {
                     if (jv >= 0) {
-                        ok = mbar_wait(bar(L::B_PFULL + r), gv & 1, ERR_SITE_PREFILL_MMA);
+                        ok = (r > 0 || wait(L::B_VFULL + vs, (gv / L::VST) & 1)) && wait(L::B_PFULL + r, gv & 1);
                         if (!ok) break;
                         if (PERSIST && jv == 0 && r == 0 && k > 0) {
                             // The first product of a tile pair overwrites O:
                             // the previous pair's epilogue must have read it.
-                            ok = mbar_wait(bar(L::B_OFREE), (k - 1) & 1, ERR_SITE_PREFILL_MMA);
+                            ok = wait(L::B_OFREE, (k - 1) & 1);
                             if (!ok) break;
                         }
                         tc_fence_after();
 #pragma unroll
-                        for (int k = 0; k < L::BN / 16; ++k) {
-                            const uint64_t bdesc = smem_desc(vsm + (uint32_t)k * 16 * 128, L::ATOM, 1024, SWZ_128B);
-                            mma_ts(tmem + o_col[r], tmem + s_col[r] + (uint32_t)k * 8, bdesc, idesc_pv,
-                                   (jv > 0 || k > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < L::BN / 16; ++kk) {
+                            const uint64_t bdesc = smem_desc(vsm + (uint32_t)kk * 16 * 128, L::ATOM, 1024, SWZ_128B);
+                            mma_ts_warp(tmem + o_col[r], tmem + s_col[r] + (uint32_t)kk * 8, bdesc, idesc_pv,
+                                        (jv > 0 || kk > 0) ? 1u : 0u);
                         }
-                        if (r == 1) mma_commit(bar(L::B_VEMPTY + vs));
+                        if (r == 1) mma_commit_warp(bar(L::B_VEMPTY + vs));
                     }
                     if (j < n_kv) {
+                        if (r == 0) {
+                            ok = wait(L::B_KFULL + ks, (gj / L::KST) & 1);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
                         const uint32_t qt = sb + L::OFF_Q + (uint32_t)r * L::Q_BYTES;
 #pragma unroll
-                        for (int k = 0; k < L::D / 16; ++k) {
-                            // K-step k: 64-column atom k / 4, 32-byte slice k % 4 within it.
-                            const uint32_t off = (uint32_t)(k >> 2) * L::ATOM + (uint32_t)(k & 3) * 32;
-                            mma_ss(tmem + s_col[r], smem_desc(qt + off, 16, 1024, SWZ_128B),
-                                   smem_desc(kst + off, 16, 1024, SWZ_128B), idesc_qk, k > 0 ? 1u : 0u);
+                        for (int kk = 0; kk < L::D / 16; ++kk) {
+                            // K-step kk: 64-column atom kk / 4, 32-byte slice kk % 4 within it.
+                            const uint32_t off = (uint32_t)(kk >> 2) * L::ATOM + (uint32_t)(kk & 3) * 32;
+                            mma_ss_warp(tmem + s_col[r], smem_desc(qt + off, 16, 1024, SWZ_128B),
+                                        smem_desc(kst + off, 16, 1024, SWZ_128B), idesc_qk, kk > 0 ? 1u : 0u);
                         }
-                        mma_commit(bar(L::B_SFULL + r));
-                        if (r == 1) mma_commit(bar(L::B_KEMPTY + ks));
-                        if (PERSIST && r == 1 && j == n_kv - 1) mma_commit(bar(L::B_QEMPTY));
+                        mma_commit_warp(bar(L::B_SFULL + r));
+                        if (r == 1) mma_commit_warp(bar(L::B_KEMPTY + ks));
+                        if (PERSIST && r == 1 && j == n_kv - 1) mma_commit_warp(bar(L::B_QEMPTY));
                     }
                 }
             }
             g += n_kv;
-            if (ok) mma_commit(bar(L::B_OFULL));
+            if (ok) mma_commit_warp(bar(L::B_OFULL));
             if constexpr (!PERSIST) break;
             }
             if (!ok) {
                 // Error: signal the epilogue anyway, and let no MMA outlive
                 // the kernel's tensor memory.
-                mma_commit(bar(L::B_OFULL));
-                mma_commit(bar(L::B_DRAIN));
+                mma_commit_warp(bar(L::B_OFULL));
+                mma_commit_warp(bar(L::B_DRAIN));
                 mbar_wait(bar(L::B_DRAIN), 0, ERR_SITE_PREFILL_DRAIN);
             }
         }

@@ -126,7 +126,9 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_cons
     using L = DecodeLayout<D, DV>;
     constexpr int CPL = DV / 32;   // dv columns per lane
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from the __shared__ array by pointer
+    // arithmetic so that every access through it stays a shared-memory access.
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -182,6 +184,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_cons
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const int* pages = reinterpret_cast<const int*>(smem + L::OFF_PAGES);
+            // Paged caches: the chunk's page (index into the staged list) and
+            // its key offset in that page, advanced chunk by chunk (key_begin
+            // and page_size are multiples of the 32-key chunk).
+            int pi = 0, off = PAGED ? key_begin - first_page * p.page_size : 0;
+            size_t page_row = 0;   // first K row of the current page for this head
+            if (PAGED && nchunks > 0) page_row = ((size_t)pages[0] * p.H + h) * p.page_size;
             int issued = 0;
             for (int c = 0; c < nchunks; ++c) {
                 const int st = c % L::NST;
@@ -192,8 +200,12 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_cons
                 // caches (the V cache has the same row order).
                 size_t krow;
                 if (PAGED) {
-                    const int pg = pages[k0 / p.page_size - first_page];
-                    krow = ((size_t)pg * p.H + h) * p.page_size + (k0 % p.page_size);
+                    krow = page_row + off;
+                    off += L::KC;
+                    if (off == p.page_size && c + 1 < nchunks) {
+                        off = 0;
+                        page_row = ((size_t)pages[++pi] * p.H + h) * p.page_size;
+                    }
                 } else {
                     krow = bh * (size_t)p.Nk + k0;
                 }

@@ -298,7 +298,9 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
               const BwdParams p) {
     using L = BwdDqLayout<D, DV>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from the __shared__ array by pointer
+    // arithmetic so that every access through it stays a shared-memory access.
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -654,7 +656,9 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                const BwdParams p) {
     using L = BwdDkvLayout<D, DV>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from the __shared__ array by pointer
+    // arithmetic so that every access through it stays a shared-memory access.
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_addr(smem);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;

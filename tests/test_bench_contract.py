@@ -1,5 +1,6 @@
 """bench.py's contract, checked on the host (no GPU): the reference arm's JSON
 line and the sha-gated traffic table that feeds roofline.traffic."""
+import hashlib
 import json
 import os
 import subprocess
@@ -37,13 +38,15 @@ def test_traffic_table_is_used_only_for_the_profiled_source(tmp_path):
         assert e["command"].count("ncu") >= 1 and "--clock-control none" in e["command"]
     e = table["entries"][0]
     src = os.path.join(ROOT, e["source"])
-    # The same record against a changed copy of its source is not used.
-    changed = tmp_path / "changed.cuh"
-    changed.write_bytes(open(src, "rb").read() + b"\n// changed\n")
+    # A record is used only while its sha256 prefix matches the source: the
+    # kernel source as profiled gives the bytes, a changed copy gives None.
     same = tmp_path / "same.cuh"
     same.write_bytes(open(src, "rb").read())
+    changed = tmp_path / "changed.cuh"
+    changed.write_bytes(open(src, "rb").read() + b"\n// changed\n")
+    sha = hashlib.sha256(same.read_bytes()).hexdigest()[:16]
     for path, expect in ((same, e["bytes_per_launch"]), (changed, None)):
         t = tmp_path / "t.json"
-        t.write_text(json.dumps({"entries": [dict(e, source=str(path))]}))
+        t.write_text(json.dumps({"entries": [dict(e, source=str(path), source_sha256_16=sha)]}))
         assert bench.traffic_from_profiles(e["kernel"], e["workload"], str(t)) == expect
     assert bench.traffic_from_profiles("no such kernel", e["workload"]) is None

@@ -222,24 +222,6 @@ __global__ void __launch_bounds__(256) bwd_finalize_kernel(const BwdParams p) {
 
 // ----------------------------------------------------------------- dQ sweep
 
-// Two 32-column TMEM loads of this thread's lane, then one wait.
-__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t (&a)[32], uint32_t tb, uint32_t (&b)[32]) {
-#define DA_R8(x, i) "=r"(x[i]), "=r"(x[i + 1]), "=r"(x[i + 2]), "=r"(x[i + 3]), "=r"(x[i + 4]), "=r"(x[i + 5]), \
-                    "=r"(x[i + 6]), "=r"(x[i + 7])
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
-        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
-        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%64];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
-        " {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47,"
-        " %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%65];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : DA_R8(a, 0), DA_R8(a, 8), DA_R8(a, 16), DA_R8(a, 24), DA_R8(b, 0), DA_R8(b, 8), DA_R8(b, 16), DA_R8(b, 24)
-        : "r"(ta), "r"(tb)
-        : "memory");
-#undef DA_R8
-}
-
 template <int D, int DV>
 struct BwdDqLayout {
     static constexpr int BM = 128;   // query rows per CTA (MMA M)

@@ -460,6 +460,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
 
         // ------------------------------------------------------------ epilogue
         g += n_kv;
+        constexpr int HALF = DV / 2;
+        const int c0 = r * HALF;
+        // Bring this thread's GroupNorm gains into L1 while the last products
+        // complete: read from L2 inside the store loop, their latency was paid
+        // once per group of columns.
+        if (p.gamma != nullptr && lane < HALF * 4 / 128)
+            prefetch_l1(p.gamma + (size_t)h * DV + c0 + lane * 32);
         if (!mbar_wait(bar(L::B_OFULL), k & 1, ERR_SITE_PREFILL_EPILOGUE)) ok = false;
         ok = __all_sync(0xffffffffu, ok);
         __syncwarp();
@@ -469,8 +476,6 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         named_barrier_sync(1, 256);
         const float inv1 = 1.0f / epi[row];
         const float inv2 = p.lambda / epi[L::BM + row];
-        constexpr int HALF = DV / 2;
-        const int c0 = r * HALF;
         const size_t rowoff = (((size_t)b * p.H + h) * p.Nq + qi) * DV + c0;
         // Training outputs for the backward pass: each map's log-sum-exp of
         // the scaled logits (natural log; m is in log2 units) and A2 V.
@@ -509,15 +514,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             tc_fence_before();
             mbar_arrive(bar(L::B_OFREE));
         }
-        float sum = 0.f;
+        float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < HALF; ++i) sum += o[i];
+        for (int i = 0; i < HALF; ++i) s4[i & 3] += o[i];
+        const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
         epi[(2 + r) * L::BM + row] = sum;
         named_barrier_sync(1, 256);
         const float mu = (epi[2 * L::BM + row] + epi[3 * L::BM + row]) * (1.0f / DV);
-        float sq = 0.f;
+        float q4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < HALF; ++i) sq += (o[i] - mu) * (o[i] - mu);
+        for (int i = 0; i < HALF; ++i) q4[i & 3] += (o[i] - mu) * (o[i] - mu);
+        const float sq = (q4[0] + q4[1]) + (q4[2] + q4[3]);
         epi[(4 + r) * L::BM + row] = sq;
         named_barrier_sync(1, 256);
         const float var = (epi[4 * L::BM + row] + epi[5 * L::BM + row]) * (1.0f / DV);
@@ -528,13 +535,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
 #pragma unroll
                 for (int i = 0; i < HALF / 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
             }
-            const float* g = p.gamma ? p.gamma + (size_t)h * DV + c0 : nullptr;
+            const float* __restrict__ g = p.gamma ? p.gamma + (size_t)h * DV + c0 : nullptr;
             uint4* dst = reinterpret_cast<uint4*>(p.out + rowoff);
 #pragma unroll
             for (int i = 0; i < HALF / 8; ++i) {
                 float y[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) y[e] = (o[8 * i + e] - mu) * sc * (g ? g[8 * i + e] : 1.0f);
+                for (int e = 0; e < 8; ++e) y[e] = (o[8 * i + e] - mu) * sc * (g ? __ldg(g + 8 * i + e) : 1.0f);
                 dst[i] = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
                                     pack_bf16x2(y[6], y[7]));
             }

@@ -388,27 +388,35 @@ def prefill_by_length(dev, reps=5):
     from transformer_attention_07_b300.workloads import WORKLOADS, make_inputs
     stream = torch.cuda.current_stream(dev)
     base = WORKLOADS["long_64k"]
-    cases = [dataclasses.replace(base, name="long_4k", B=16, Nq=4096, Nk=4096),
+    # The causal 2K and cancellation workloads at their own shapes (B4 H8 N2048,
+    # B2 H16 N8192, with their own inputs), the 4K and 16K points of the 64K
+    # distributions at its token count, and the 128K workload.
+    cases = [WORKLOADS["causal_2k"], WORKLOADS["cancel_8k"],
+             dataclasses.replace(base, name="long_4k", B=16, Nq=4096, Nk=4096),
              dataclasses.replace(base, name="long_16k_b4", B=4, Nq=16384, Nk=16384),
              WORKLOADS["long_128k"]]
+    peak, _, _, src = load_peaks()
     res = {}
     for w in cases:
         inp = make_inputs(w, device=dev)
         out = torch.empty((w.B, w.H, w.Nq, w.dv), dtype=torch.bfloat16, device=dev)
         run = lambda: da.fwd(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], w.lam, w.lam_init,
                              causal=w.causal, gamma=inp["gamma"], eps=w.eps, out=out, stream=stream)
+        n_rep = reps if w.Nq >= 16384 else 10 * reps   # short launches: more of them per timing
         for _ in range(3):
             run()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(reps):
+        for _ in range(n_rep):
             run()
         e1.record(stream)
         torch.cuda.synchronize(dev)
         if da.last_device_error() != 0:
             raise RuntimeError(f"device-side error in the prefill at {w.name}")
-        ms = e0.elapsed_time(e1) / reps
-        res[w.name] = {"B": w.B, "H": w.H, "N": w.Nq, "ms": ms, "TFLOP/s": w.flops / (ms * 1e-3) / 1e12}
+        ms = e0.elapsed_time(e1) / n_rep
+        tflops = w.flops / (ms * 1e-3) / 1e12
+        res[w.name] = {"B": w.B, "H": w.H, "N": w.Nq, "ms": ms, "TFLOP/s": tflops, "frac": tflops / peak,
+                       "peak_source": f"{src} burst"}
         del inp, out
         torch.cuda.empty_cache()
     return res

@@ -94,8 +94,11 @@ struct PrefillLayout {
     static constexpr int B_VFULL = B_KEMPTY + KST;
     static constexpr int B_VEMPTY = B_VFULL + VST;
     static constexpr int B_SFULL = B_VEMPTY + VST;   // 2 (one per map)
-    static constexpr int B_PFULL = B_SFULL + 2;      // 4: map r, half hh (keys 64 hh .. 64 hh + 63) at 2 r + hh
-    static constexpr int B_OFULL = B_PFULL + 4;
+    // P is handed to the issuer in PSPLIT parts of BN / PSPLIT keys each.
+    static constexpr int PSPLIT = 2;
+    static constexpr int PKEYS = BN / PSPLIT;
+    static constexpr int B_PFULL = B_SFULL + 2;      // 2 PSPLIT: map r, part hh at PSPLIT r + hh
+    static constexpr int B_OFULL = B_PFULL + 2 * PSPLIT;
     static constexpr int B_OFREE = B_OFULL + 1;      // persistent: O read by the epilogue (count 256)
     static constexpr int B_QEMPTY = B_OFREE + 1;     // persistent: Q tiles no longer read
     static constexpr int B_DRAIN = B_QEMPTY + 1;     // issuer: every issued MMA complete (error path)
@@ -174,8 +177,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         }
         for (int r = 0; r < 2; ++r) {
             mbar_init(bar(L::B_SFULL + r), 1);
-            mbar_init(bar(L::B_PFULL + 2 * r), 128);
-            mbar_init(bar(L::B_PFULL + 2 * r + 1), 128);
+            for (int hh = 0; hh < L::PSPLIT; ++hh) mbar_init(bar(L::B_PFULL + L::PSPLIT * r + hh), 128);
         }
         mbar_init(bar(L::B_OFULL), 1);
         mbar_init(bar(L::B_OFREE), 256);
@@ -274,12 +276,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             constexpr uint64_t K2_OFF = L::K_BYTES >> 4, KSTAGE = (2 * L::K_BYTES) >> 4, VSTAGE = L::V_BYTES >> 4;
             const uint32_t t_s1 = tmem + L::TM_S1, t_s2 = tmem + L::TM_S2;
             const uint32_t t_o1 = tmem + L::TM_O1, t_o2 = tmem + L::TM_O2;
-            // O += P V over half hh of one key tile (keys 64 hh .. 64 hh + 63):
-            // 16-key steps, P from TMEM columns 8k.
+            // O += P V over part hh of one key tile (keys PKEYS hh .. PKEYS
+            // (hh + 1) - 1): 16-key steps, P from TMEM columns 8k.
             auto pv = [&](uint32_t t_o, uint32_t t_p, uint64_t dvs, uint32_t acc0, int hh) {
 #pragma unroll
-                for (int kk = 0; kk < L::BN / 32; ++kk) {
-                    const int k = hh * (L::BN / 32) + kk;
+                for (int kk = 0; kk < L::PKEYS / 16; ++kk) {
+                    const int k = hh * (L::PKEYS / 16) + kk;
                     mma_ts_warp(t_o, t_p + 8u * k, dvs + (uint64_t)(k * (16 * 128 >> 4)), idesc_pv,
                                 k == 0 ? acc0 : 1u);
                 }
@@ -327,10 +329,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                         }
                         tc_fence_after();
                         pv(t_o1, t_s1, dvs, acc0, 0);
-                        ok = wait(L::B_PFULL + 1, gv & 1);
+#pragma unroll
+                        for (int hh = 1; hh < L::PSPLIT && ok; ++hh) {
+                            ok = wait(L::B_PFULL + hh, gv & 1);
+                            tc_fence_after();
+                            if (ok) pv(t_o1, t_s1, dvs, acc0, hh);
+                        }
                         if (!ok) break;
-                        tc_fence_after();
-                        pv(t_o1, t_s1, dvs, acc0, 1);
                     }
                     if (j < n_kv) {
                         ok = wait(L::B_KFULL + ks, (gj / L::KST) & 1);
@@ -341,14 +346,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                     }
                     // map 2
                     if (jv >= 0) {
-                        ok = wait(L::B_PFULL + 2, gv & 1);
+#pragma unroll
+                        for (int hh = 0; hh < L::PSPLIT && ok; ++hh) {
+                            ok = wait(L::B_PFULL + L::PSPLIT + hh, gv & 1);
+                            tc_fence_after();
+                            if (ok) pv(t_o2, t_s2, dvs, acc0, hh);
+                        }
                         if (!ok) break;
-                        tc_fence_after();
-                        pv(t_o2, t_s2, dvs, acc0, 0);
-                        ok = wait(L::B_PFULL + 3, gv & 1);
-                        if (!ok) break;
-                        tc_fence_after();
-                        pv(t_o2, t_s2, dvs, acc0, 1);
                         mma_commit_warp(bar(L::B_VEMPTY + vs));
                     }
                     if (j < n_kv) {
@@ -431,18 +435,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             // so a row dominated by one key keeps that key's rounding out of
             // O/l; four packed chains.
             const float nm = (m == -INFINITY) ? 0.f : -m;
-            // P goes to the issuer in two halves of 64 keys: the P V of the
-            // first half runs while the second half's exponentials are
-            // computed.  The rare O rescale happens before the first half is
-            // handed over (the first half's P V accumulates into O); the
-            // previous P_r V has completed (it was issued before this tile's
-            // S_r, whose commit we waited on).
+            // P goes to the issuer in PSPLIT parts: the P V of a part runs
+            // while the next part's exponentials are computed.  The rare O
+            // rescale happens before the first part is handed over (that
+            // part's P V accumulates into O); the previous P_r V has
+            // completed (it was issued before this tile's S_r, whose commit
+            // we waited on).
+            constexpr int PK = L::PKEYS;
             float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f, a4 = 0.f, a5 = 0.f, a6 = 0.f, a7 = 0.f;
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t pk[32];
+            for (int hh = 0; hh < L::PSPLIT; ++hh) {
+                uint32_t pk[PK / 2];
 #pragma unroll
-                for (int i = 64 * hh; i < 64 * hh + 64; i += 8) {
+                for (int i = PK * hh; i < PK * hh + PK; i += 8) {
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; e += 2)
@@ -452,13 +457,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                     for (int e = 0; e < 8; ++e) x[e] = fast_exp2(x[e]);
                     uint32_t w[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) pk[((i - 64 * hh) >> 1) + e] = w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
+                    for (int e = 0; e < 4; ++e) pk[((i - PK * hh) >> 1) + e] = w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
                     acc_bf16x2(a0, a1, w[0]);
                     acc_bf16x2(a2, a3, w[1]);
                     acc_bf16x2(a4, a5, w[2]);
                     acc_bf16x2(a6, a7, w[3]);
                 }
-                tmem_st32(tmem + t_lane + s_col + 32u * hh, pk);
+                if constexpr (PK == 64)
+                    tmem_st32(tmem + t_lane + s_col + 32u * hh, pk);
+                else
+                    tmem_st16(tmem + t_lane + s_col + 16u * hh, pk);
                 if (hh == 0 && rescale) {
 #pragma unroll
                     for (int c = 0; c < DV / 32; ++c) {
@@ -471,7 +479,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                 }
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(L::B_PFULL + 2 * r + hh));
+                mbar_arrive(bar(L::B_PFULL + L::PSPLIT * r + hh));
             }
             l += ((a0 + a1) + (a2 + a3)) + ((a4 + a5) + (a6 + a7));
         }

@@ -134,6 +134,11 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tm_k1, const __grid_cons
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const size_t bh = (size_t)b * p.H + h;
+    // Launched as a dependent grid: the inputs, and the partials buffer that
+    // the previous call's merge may still be reading, are touched only after
+    // the previous grid on the stream has completed.
+    grid_dependency_wait();
+    grid_launch_dependents();
     int seq_len = p.Nk;
     if (PAGED) {
         // Lengths and pages come from device memory the host cannot check:
@@ -329,6 +334,10 @@ decode_merge_kernel(const MergeParams p) {
     constexpr int CPL = DV / 32;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t bh = (size_t)blockIdx.x * 4 + warp;
+    // Launched as a dependent grid of the split kernel: its partials are read
+    // only once that grid has completed.
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (bh >= (size_t)p.B * p.H) return;
     const int h = (int)(bh % p.H);
     // Partial t = (part, split) of this head: parts are [parts][B*H][S] blocks.

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <utility>
 
 #include "launch.h"
 #include "sm103_ptx.cuh"
@@ -315,6 +316,27 @@ int launch_standard(const StandardArgs& a, cudaStream_t st) {
 
 // ----------------------------------------------------------------- decode
 
+// Launches a decode kernel as a dependent grid (programmatic stream
+// serialisation): it may be scheduled while the previous grid on the stream
+// drains, and waits for that grid's completion inside the kernel before it
+// touches memory.  The split and merge kernels of one call then follow each
+// other without a full launch gap.
+template <typename... Params, typename... Args>
+static cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 template <int D, int DV, bool PAGED>
 static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     using L = DecodeLayout<D, DV>;
@@ -346,8 +368,9 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
                  "decode: set shared memory"))
         return LAUNCH_ERR_CUDA;
-    kern<<<dim3(a.splits, a.H, a.B), L::THREADS, L::SMEM_BYTES, st>>>(mk1, mk2, p);
-    if (!cuda_ok(cudaGetLastError(), "decode: split launch")) return LAUNCH_ERR_CUDA;
+    if (!cuda_ok(launch_dependent(kern, dim3(a.splits, a.H, a.B), dim3(L::THREADS), L::SMEM_BYTES, st, mk1, mk2, p),
+                 "decode: split launch"))
+        return LAUNCH_ERR_CUDA;
     if (a.partials_only) return LAUNCH_OK;
     MergeParams mp;
     mp.B = a.B;
@@ -362,8 +385,10 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     mp.out = static_cast<uint16_t*>(a.out);
     mp.o_prenorm = a.o_prenorm;
     const int heads = a.B * a.H;
-    decode_merge_kernel<DV><<<(heads + 3) / 4, 128, 0, st>>>(mp);
-    return cuda_ok(cudaGetLastError(), "decode: merge launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+    return cuda_ok(launch_dependent(decode_merge_kernel<DV>, dim3((heads + 3) / 4), dim3(128), 0, st, mp),
+                   "decode: merge launch")
+               ? LAUNCH_OK
+               : LAUNCH_ERR_CUDA;
 }
 
 int launch_decode_merge(const MergeArgs& a, cudaStream_t st) {
@@ -380,13 +405,14 @@ int launch_decode_merge(const MergeArgs& a, cudaStream_t st) {
     mp.out = static_cast<uint16_t*>(a.out);
     mp.o_prenorm = a.o_prenorm;
     const int heads = a.B * a.H;
+    cudaError_t e;
     if (a.dv == 128)
-        decode_merge_kernel<128><<<(heads + 3) / 4, 128, 0, st>>>(mp);
+        e = launch_dependent(decode_merge_kernel<128>, dim3((heads + 3) / 4), dim3(128), 0, st, mp);
     else if (a.dv == 64)
-        decode_merge_kernel<64><<<(heads + 3) / 4, 128, 0, st>>>(mp);
+        e = launch_dependent(decode_merge_kernel<64>, dim3((heads + 3) / 4), dim3(128), 0, st, mp);
     else
         return LAUNCH_ERR_UNSUPPORTED;
-    return cuda_ok(cudaGetLastError(), "decode: merge of gathered partials") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+    return cuda_ok(e, "decode: merge of gathered partials") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }
 
 int launch_decode(const DecodeArgs& a, cudaStream_t st) {

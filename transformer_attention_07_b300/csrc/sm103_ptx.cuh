@@ -111,6 +111,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // Fetch the 128-byte line holding `p` into L1 (no register result).
+// Programmatic dependent launch.  A grid launched with programmatic stream
+// serialisation may be scheduled before the previous grid on its stream has
+// ended.  grid_dependency_wait() returns once every prerequisite grid has
+// completed and its memory operations are visible (at once for a grid launched
+// without the attribute); nothing a prerequisite writes may be read or
+// overwritten before it.  grid_launch_dependents() lets the next such grid be
+// scheduled once every CTA of this one has called it or exited; it orders no
+// memory.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_l1(const void* p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }

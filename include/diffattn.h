@@ -196,6 +196,22 @@ int diffattn_standard_fwd(const void* q, const void* k, const void* v, int causa
 size_t diffattn_decode_workspace_bytes(int B, int H, int Nk, int dv, int num_splits);
 
 /*
+ * The key-range count diffattn_decode, diffattn_decode_paged (with Nk =
+ * max_pages * page_size) and diffattn_decode_noalloc use when num_splits = 0,
+ * for a device with `sms` streaming multiprocessors (148 on a B300).  Pure
+ * host arithmetic, no CUDA call:
+ *   * it minimises a cost model of the split kernel: each wave of CTAs costs a
+ *     fixed start-up worth about 128 KB of streaming, plus its largest key
+ *     range streamed at the per-SM share of HBM bandwidth (up to 1.3 times
+ *     that share when the wave leaves SMs idle);
+ *   * ranges are whole 32-key chunks, none empty, at least 256 keys;
+ *   * max_splits caps the count (0 = the default cap of 32; at most 64);
+ *     the no-alloc entry point passes what its scratch holds.
+ * Returns 0 for invalid arguments or unsupported widths.
+ */
+int diffattn_decode_auto_splits(int B, int H, int Nk, int d, int dv, int sms, int max_splits);
+
+/*
  * Split-KV decode: one query per (b, h) against a key/value cache of Nk rows,
  * no mask (the same operation as diffattn_fwd with Nq = 1, causal = 0).
  *   q1, q2      [B,H,1,d] bf16;  k1, k2 [B,H,Nk,d] bf16;  v [B,H,Nk,dv] bf16

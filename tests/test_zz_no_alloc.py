@@ -12,8 +12,7 @@ scratch keeps the previous call's contents), and check:
   * bit for bit against the workspace entry point (diffattn_decode) when both
     run the same split count: the same kernels on the same partials layout;
   * against the fp64 oracle, on every head of the smaller problems and on
-    sampled heads of the one whose automatic split count must be capped to
-    fit the scratch;
+    sampled heads of a 300-head problem in automatic mode;
   * that the free device memory does not change across the calls;
   * that a problem too large for the scratch, even at one split, is refused
     without a launch.
@@ -127,15 +126,20 @@ def test_noalloc_equals_workspace_entry_point_bitwise_and_matches_oracle():
         assert np.abs(flat(out, heads) - y_ref).max() <= TOL_OUT
 
 
-def test_noalloc_caps_the_automatic_split_count_to_its_scratch():
-    """B=1, H=300, Nk=16384: on 148 SMs the workspace entry point picks 27
-    key ranges per head (8.55 MB of partials, more than the scratch); the
-    no-alloc call must pick a count that fits and still compute the result."""
+def test_noalloc_automatic_split_count_fits_and_matches_the_workspace_entry_point():
+    """B=1, H=300, Nk=16384 with num_splits = 0: the no-alloc call picks its
+    key-range count with the workspace entry point's model, capped to what
+    the scratch holds (26 ranges here).  The model's pick fits, so both entry
+    points run the same count and must agree bit for bit.  (The cap itself is
+    host arithmetic, checked without a GPU through diffattn_decode_auto_splits.)"""
     B, H, Nk, d, dv = 1, 300, 16384, 64, 128
     per_split = B * H * 2 * (dv + 4) * 4
-    assert 27 * per_split > SCRATCH_BYTES >= per_split
+    fit = SCRATCH_BYTES // per_split
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    auto = da.decode_auto_splits(B, H, Nk, d, dv, sms)
+    assert auto == da.decode_auto_splits(B, H, Nk, d, dv, sms, min(fit, 32))
     inp = random_cache(B, H, Nk, d, dv, 25)
-    _, ref_pre = run_workspace(inp, 0.6, 0.8, 0)
+    ref_out, ref_pre = run_workspace(inp, 0.6, 0.8, 0)
     outputs = [nan_outputs(inp) for _ in range(2)]
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
@@ -147,10 +151,9 @@ def test_noalloc_caps_the_automatic_split_count_to_its_scratch():
         assert da.last_device_error() == 0
         outs.append((out, pre))
     assert torch.cuda.mem_get_info()[0] == free0
-    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    for out, pre in outs:
+        assert torch.equal(out, ref_out) and torch.equal(pre, ref_pre)
     out, pre = outs[1]
-    # Another split count only changes the fp32 summation order.
-    assert (pre - ref_pre).abs().max().item() < 1e-5
     heads = torch.randperm(B * H, generator=torch.Generator().manual_seed(26))[:32].tolist()
     o_ref, y_ref = oracle_heads(inp, 0.6, 0.8, heads)
     assert np.abs(flat(pre, heads) - o_ref).max() <= TOL_PRE

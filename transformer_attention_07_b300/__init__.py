@@ -19,7 +19,7 @@ import os
 
 __all__ = [
     "fwd", "fwd_host", "fwd_host_workspace_bytes", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes",
-    "standard_fwd", "decode", "decode_paged", "decode_workspace_bytes", "decode_partials", "decode_partials_bytes",
+    "standard_fwd", "decode", "decode_paged", "decode_workspace_bytes", "decode_auto_splits", "decode_partials", "decode_partials_bytes",
     "decode_merge", "gather_partials", "decode_sharded", "head_range", "gather_heads", "fwd_sharded",
     "status_string", "last_device_error", "selftest_wait_timeout", "load", "LIB_PATH",
     "DiffAttnError", "SUPPORTED_WIDTHS",
@@ -57,6 +57,8 @@ def load():
     lib.diffattn_fwd_ex.restype = i32
     lib.diffattn_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.diffattn_decode_workspace_bytes.restype = sz
+    lib.diffattn_decode_auto_splits.argtypes = [i32, i32, i32, i32, i32, i32, i32]
+    lib.diffattn_decode_auto_splits.restype = i32
     lib.diffattn_decode.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, vp, f32, i32, vp, sz,
                                     vp, vp, vp]
     lib.diffattn_decode.restype = i32
@@ -295,6 +297,12 @@ def standard_fwd(q, k, v, causal=False, out=None, out_f32=None, stream=None):
 
 def decode_workspace_bytes(B, H, Nk, dv, num_splits=0) -> int:
     return int(load().diffattn_decode_workspace_bytes(B, H, Nk, dv, num_splits))
+
+
+def decode_auto_splits(B, H, Nk, d, dv, sms, max_splits=0) -> int:
+    """Key ranges per (b, h) the decode entry points use with num_splits = 0 on
+    a device with ``sms`` SMs (host arithmetic; 0 for invalid arguments)."""
+    return int(load().diffattn_decode_auto_splits(B, H, Nk, d, dv, sms, max_splits))
 
 
 def decode(q1, k1, q2, k2, v, lam, lam_init, gamma=None, eps=1e-5, num_splits=0, workspace=None, out=None,

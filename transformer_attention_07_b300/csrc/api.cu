@@ -3,6 +3,7 @@
 // nothing when one is wrong; the launchers in kernels.cu do the rest.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -59,25 +60,44 @@ size_t workspace_for(int B, int H, int dv, int splits) {
     return (size_t)B * (size_t)H * (size_t)splits * 2u * (size_t)(dv + 4) * sizeof(float);
 }
 
-// Key ranges per (b, h): enough CTAs to fill the GPU in whole waves, at
-// least 512 keys per range, and at most max_splits ranges.
-int choose_splits(int64_t heads, int Nk, int sms, int max_splits = kMaxAutoSplits) {
-    const int by_keys = (int)((Nk + 511) / 512);
-    int cap = by_keys < max_splits ? by_keys : max_splits;
-    if (cap < 1) cap = 1;
+// Key ranges per (b, h): the count that minimises a cost model of the split
+// kernel, fitted to B300 timings of B1-B8, H8-H32 and 1K-32K keys.
+//   * One CTA streams one key range.  In a wave that occupies every SM, a CTA
+//     gets the fair per-SM share of HBM bandwidth; in a wave with idle SMs it
+//     gets up to 1.3 times that share (measured: 55-60 GB/s per CTA against
+//     44 GB/s).
+//   * Every wave adds a fixed cost (CTA start, the first loads' latency, the
+//     partials' write) worth about 128 KB of streaming (3 us).
+//   * Ranges are whole 32-key chunks, none empty, at least 256 keys, and at
+//     most max_splits.  A count must beat the previous best by 1% to be taken,
+//     so ties go to fewer ranges (less merge work).
+// Filling whole waves with many short ranges, the previous rule, cost up to
+// 40% at B4 H32 with 4K keys.
+int choose_splits(int64_t heads, int Nk, int bytes_per_key, int sms, int max_splits = kMaxAutoSplits) {
+    if (heads < 1 || Nk < 1 || sms < 1) return 1;
+    constexpr double kWaveCost = 128.0 * 1024.0;   // bytes
+    constexpr double kIdleBoost = 1.3;
+    const int by_keys = (Nk + 255) / 256;
+    const int cap = std::max(1, std::min(by_keys, max_splits));
     int best = 1;
-    double best_eff = -1.0;
+    double best_cost = -1.0;
     for (int s = 1; s <= cap; ++s) {
-        const double ctas = (double)heads * s;
-        const double waves = std::ceil(ctas / sms);
-        const double eff = ctas / (waves * sms);
-        if (eff > best_eff + 0.01) {
+        const int per = ((Nk + s - 1) / s + 31) / 32 * 32;
+        if ((int64_t)(s - 1) * per >= Nk) continue;   // the last range would be empty
+        const double bytes = (double)per * bytes_per_key;
+        const int64_t ctas = heads * s;
+        const int64_t full = ctas / sms, rem = ctas % sms;
+        double cost = (double)full * (kWaveCost + bytes);
+        if (rem) cost += kWaveCost + bytes * std::max(1.0 / kIdleBoost, (double)rem / sms);
+        if (best_cost < 0.0 || cost < 0.99 * best_cost) {
             best = s;
-            best_eff = eff;
+            best_cost = cost;
         }
     }
     return best;
 }
+
+int key_bytes(int d, int dv) { return (2 * d + dv) * 2; }
 
 // Streaming multiprocessors of the current device, or 0 if the runtime cannot say.
 int device_sms() {
@@ -222,6 +242,12 @@ int diffattn_standard_fwd(const void* q, const void* k, const void* v, int causa
     return from_launch(diffattn::launch_standard(a, static_cast<cudaStream_t>(stream)));
 }
 
+int diffattn_decode_auto_splits(int B, int H, int Nk, int d, int dv, int sms, int max_splits) {
+    if (B < 1 || H < 1 || Nk < 1 || sms < 1 || max_splits < 0 || max_splits > kMaxSplits) return 0;
+    if (!supported_widths(d, dv)) return 0;
+    return choose_splits((int64_t)B * H, Nk, key_bytes(d, dv), sms, max_splits == 0 ? kMaxAutoSplits : max_splits);
+}
+
 size_t diffattn_decode_workspace_bytes(int B, int H, int Nk, int dv, int num_splits) {
     if (B < 0 || H < 0 || Nk < 1 || dv < 1 || num_splits < 0 || num_splits > kMaxSplits) return 0;
     return workspace_for(B, H, dv, num_splits == 0 ? kMaxAutoSplits : num_splits);
@@ -239,7 +265,7 @@ int diffattn_decode(const void* q1, const void* k1, const void* q2, const void* 
     if (splits == 0) {
         const int sms = device_sms();
         if (sms < 1) return DIFFATTN_ERR_CUDA;
-        splits = choose_splits((int64_t)B * H, Nk, sms);
+        splits = choose_splits((int64_t)B * H, Nk, key_bytes(d, dv), sms);
     }
     return decode_with_splits(q1, k1, q2, k2, v, lambda, lambda_init, B, H, Nk, d, dv, gn_gamma, eps, splits,
                               workspace, workspace_bytes, out, o_prenorm, stream);
@@ -310,7 +336,8 @@ int diffattn_decode_noalloc(const void* q1, const void* k1, const void* q2, cons
     if (splits == 0) {
         const int sms = device_sms();
         if (sms < 1) return DIFFATTN_ERR_CUDA;
-        splits = choose_splits((int64_t)B * H, Nk, sms, fit < (size_t)kMaxAutoSplits ? (int)fit : kMaxAutoSplits);
+        splits = choose_splits((int64_t)B * H, Nk, key_bytes(d, dv), sms,
+                               fit < (size_t)kMaxAutoSplits ? (int)fit : kMaxAutoSplits);
     }
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
@@ -355,7 +382,7 @@ int diffattn_decode_paged(const void* q1, const void* q2, const void* k1_pages, 
                                "paged decode: SM count") ||
             sms < 1)
             return DIFFATTN_ERR_CUDA;
-        splits = choose_splits((int64_t)B * H, max_len, sms);
+        splits = choose_splits((int64_t)B * H, max_len, key_bytes(d, dv), sms);
         while (!pages_ok(splits) && splits < kMaxSplits) ++splits;
     }
     if (!pages_ok(splits)) return DIFFATTN_ERR_INVALID_ARG;

@@ -27,11 +27,13 @@
 //                       S_r = Q_r K_r^T, dP = dO V^T on the tensor core,
 //                       dS_r in registers, dQ_r += dS_r K_r (dS_r from TMEM);
 //                       the next tile's scores follow each map's dQ product.
-//   bwd_dkv_kernel      one CTA per 128 keys; walks 128-query tiles:
+//   bwd_dkv_kernel      one CTA per 128 keys; walks the query tiles in
+//                       64-query units through two tensor-memory slots:
 //                       S_r^T = K_r Q_r^T, dP^T = V dO^T, then
-//                       dV += (A1 - lambda A2)^T dO, dK_r += dS_r^T Q_r,
-//                       the dS arithmetic in 16-query chunks that overlap
-//                       the previous chunk's products.
+//                       dV += (A1 - lambda A2)^T dO, dK_r += dS_r^T Q_r;
+//                       one unit's products run while the dS warps work on
+//                       the other, the dS arithmetic in 16-query chunks that
+//                       overlap the previous chunk's products.
 //   bwd_finalize_kernel the dgamma and dlambda sums, in a fixed order.
 // dQ and dK/dV come from separate sweeps (the dQ sweep recomputes S and dP),
 // so every gradient is written once, by one CTA, without atomics: results
@@ -567,10 +569,32 @@ bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 
 // ----------------------------------------------------------------- dK/dV sweep
 
+// N fp32 columns of this thread's TMEM lane, times s, rounded to bf16 and
+// stored to dst (16-byte aligned) when `store`; the load runs on every lane.
+template <int N>
+__device__ __forceinline__ void tmem_cols_to_bf16(uint32_t taddr, uint16_t* dst, float s, bool store) {
+    static_assert(N == 16 || N == 32, "column count");
+    uint32_t a[N];
+    if constexpr (N == 16)
+        tmem_ld16(taddr, a);
+    else
+        tmem_ld32(taddr, a);
+    if (store) {
+        uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int i = 0; i < N / 8; ++i)
+            d4[i] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * i]) * s, __uint_as_float(a[8 * i + 1]) * s),
+                               pack_bf16x2(__uint_as_float(a[8 * i + 2]) * s, __uint_as_float(a[8 * i + 3]) * s),
+                               pack_bf16x2(__uint_as_float(a[8 * i + 4]) * s, __uint_as_float(a[8 * i + 5]) * s),
+                               pack_bf16x2(__uint_as_float(a[8 * i + 6]) * s, __uint_as_float(a[8 * i + 7]) * s));
+    }
+}
+
 template <int D, int DV>
 struct BwdDkvLayout {
     static constexpr int BK = 128;   // keys per CTA (MMA M)
-    static constexpr int BQ = 128;   // query rows per tile (MMA N of the score products)
+    static constexpr int BQ = 128;   // query rows per staged tile
+    static constexpr int BU = 64;    // query rows per unit: half a staged tile (MMA N of S^T and dP^T)
     static constexpr int QST = 2;    // ring depth of (Q1, Q2, dO, row constants)
     static constexpr uint32_t K_BYTES = BK * D * 2;
     static constexpr uint32_t V_BOX = BK * 128;
@@ -586,32 +610,39 @@ struct BwdDkvLayout {
     static constexpr uint32_t OFF_V = 2 * K_BYTES;
     static constexpr uint32_t OFF_Q = OFF_V + V_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_Q + QST * STAGE;
+    // dS warps: one per TMEM lane quarter in each of NG column groups of a unit.
+    static constexpr int NG = 2;
+    static constexpr int GC = BU / NG;               // columns per group (32)
+    static constexpr int NDS = 4 * NG;               // dS warps
+    static constexpr int CW = 16;                    // queries per chunk: one k-step of the gradient products
+    static constexpr int NCH = GC / CW;              // chunks per group
     static constexpr int B_KV = 0;
     static constexpr int B_QFULL = 1;
     static constexpr int B_QEMPTY = B_QFULL + QST;
-    static constexpr int B_S1FULL = B_QEMPTY + QST;   // S1^T (and S2^T issued behind it) in flight
-    static constexpr int B_S1FREE = B_S1FULL + 1;     // the dS warps hold S1^T in registers
-    static constexpr int B_DPFULL = B_S1FREE + 1;     // S2^T and dP^T complete
-    static constexpr int NCH = 4;                    // chunks per half of the tile
-    static constexpr int CW = 64 / NCH;              // queries per chunk (16 or 32)
-    static constexpr int B_PFULL = B_DPFULL + 1;      // [chunk]: bf16 operands of one chunk of both halves
-    static constexpr int B_DONE = B_PFULL + NCH;
+    static constexpr int B_SFULL = B_QEMPTY + QST;   // [slot]: S1^T and S2^T of the slot's unit complete
+    static constexpr int B_SFREE = B_SFULL + 2;      // [slot]: the dS warps hold both in registers
+    static constexpr int B_DPFULL = B_SFREE + 2;     // [slot]: dP^T complete
+    static constexpr int B_PFULL = B_DPFULL + 2;     // [slot][chunk]: bf16 operands of one chunk of every group
+    static constexpr int B_GDONE = B_PFULL + 2 * NCH;   // [slot]: the slot's gradient products complete
+    static constexpr int B_DONE = B_GDONE + 2;
     static constexpr int NBAR = B_DONE + 1;
     static constexpr uint32_t OFF_TMEM_SLOT = OFF_BAR + NBAR * 8;
     static constexpr uint32_t USED = OFF_TMEM_SLOT + 16;
     // +1024 for aligning the dynamic base; at least 120 KB so that a single
     // CTA (which takes all 512 TMEM columns) is resident per SM.
     static constexpr uint32_t SMEM_BYTES = (USED + 1024 > 120u * 1024u) ? USED + 1024 : 120u * 1024u;
-    // Tensor memory: the dV, dK1, dK2 accumulators (dv + 2d columns), then
-    // two 128-column score regions.  Region A holds S1^T, then dP^T, then the
-    // bf16 dS1^T and dS2^T; region B holds S2^T, then the bf16
-    // (A1 - lambda A2)^T.  In bf16 each chunk of CW queries packs inside
-    // the columns its own fp32 values came from: dS1^T then dS2^T (CW / 2
-    // columns each) in region A, (A1 - lambda A2)^T in the first CW / 2 of
-    // region B.
-    static constexpr uint32_t TM_DV = 0, TM_DK1 = DV, TM_DK2 = DV + D, TM_A = 256, TM_B = 384;
+    // Tensor memory: the dV, dK1, dK2 accumulators (dv + 2d columns), then two
+    // unit slots of 128 columns.  Slot h takes the units of query rows
+    // [64 h, 64 h + 64) of each staged tile.  Its region A (64 columns) holds
+    // S1^T, then dP^T, then the bf16 dS1^T and dS2^T; its region B (64
+    // columns) holds S2^T, then the bf16 (A1 - lambda A2)^T.  In bf16 each
+    // 16-query chunk packs inside the columns its own fp32 values came from:
+    // dS1^T then dS2^T (8 columns each) in region A, (A1 - lambda A2)^T in the
+    // first 8 of the chunk's columns of region B.
+    static constexpr uint32_t TM_DV = 0, TM_DK1 = DV, TM_DK2 = DV + D, TM_SLOTS = 256;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr int THREADS = 320;
+    static constexpr int W_GRAD = 2 + NDS;           // the warp that issues the gradient products
+    static constexpr int THREADS = 96 + 32 * NDS;   // producer, score/dP issuer, dS warps, gradient issuer
     // Q/K rows are one swizzle span wide (128 or 64 bytes); dO and V come in
     // 64-column boxes of 128-byte rows.
     static constexpr uint32_t QK_ROW = D * 2;
@@ -619,19 +650,31 @@ struct BwdDkvLayout {
     static constexpr uint32_t QK_SBO = 8 * QK_ROW;
     static_assert((D == 64 && DV == 128) || (D == 32 && DV == 64), "backward widths");
     static_assert(STAGE % 1024 == 0, "stage layout");
-    static_assert(DV + 2 * D <= TM_A, "accumulators below the score regions");
+    static_assert(DV + 2 * D <= TM_SLOTS, "accumulators below the unit slots");
+    static_assert((BU * QK_ROW) % 1024 == 0 && (BU * 128) % 1024 == 0, "unit offsets keep the swizzle atoms");
     static_assert(SMEM_BYTES <= 227u * 1024u && SMEM_BYTES > 114u * 1024u, "one CTA per SM");
 };
 
-// One CTA owns 128 keys and walks the 128-query tiles that see them.  Per
-// tile the tensor core computes S1^T = K1 Q1^T and S2^T = K2 Q2^T (M = 128
-// keys, N = 128 queries), then dP^T = V dO^T into S1^T's columns once the dS
-// warps hold S1^T; the dS warps (two per TMEM lane quarter, 64 queries each)
-// form A1^T, then A2^T, dS1^T, dS2^T and (A1 - lambda A2)^T in four 16-query
-// chunks, and the gradient products dV += (A1 - lambda A2)^T dO,
-// dK_r += dS_r^T Q_r of chunk c run while chunk c + 1 is computed.
+// One CTA owns 128 keys and walks the 128-query tiles that see them, half a
+// tile (a 64-query unit) at a time, with two unit slots in tensor memory so
+// that one unit's products run while the dS warps work on the other.
+//   * Per unit the tensor core computes S1^T = K1 Q1^T and S2^T = K2 Q2^T
+//     (M = 128 keys, N = 64 queries).
+//   * The dS warps (two per TMEM lane quarter, 32 queries each) take both
+//     into registers and release the slot; dP^T = V dO^T then goes over
+//     S1^T while the dS warps form A1^T and A2^T.
+//   * From dP^T, in 16-query chunks, they form dS1^T, dS2^T and
+//     (A1 - lambda A2)^T in bf16; the gradient products
+//     dV += (A1 - lambda A2)^T dO and dK_r += dS_r^T Q_r of chunk c run while
+//     chunk c + 1 is computed.
+//   * Two warps issue: one the score and dP^T products, one the gradient
+//     products, so that dP^T of unit u + 1 goes in as soon as the dS warps
+//     hold its scores, whatever gradient products are still queued.  The
+//     scores of unit u + 2 go into unit u's slot once a barrier committed
+//     behind unit u's gradient products reports them complete.
+
 template <int D, int DV, bool CAUSAL>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(BwdDkvLayout<D, DV>::THREADS, 1)
 bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
                const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_k1,
                const __grid_constant__ CUtensorMap tm_k2, const __grid_constant__ CUtensorMap tm_v,
@@ -650,9 +693,10 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
     const int k0 = kt * L::BK;
     const int diag = p.Nk - p.Nq;
     // Query tiles that see at least one of this CTA's keys: key j is seen by
-    // query i iff j <= i + diag.
+    // query i iff j <= i + diag.  Unit u is half u % 2 of tile u / 2.
     const int t0 = CAUSAL ? max(0, k0 - diag) / L::BQ : 0;
     const int n_t = (p.Nq + L::BQ - 1) / L::BQ - t0;
+    const int n_u = 2 * n_t;
 
     auto bar = [&](int i) -> uint32_t { return sb + L::OFF_BAR + 8u * (uint32_t)i; };
 
@@ -662,10 +706,13 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             mbar_init(bar(L::B_QFULL + s), 1);
             mbar_init(bar(L::B_QEMPTY + s), 1);
         }
-        mbar_init(bar(L::B_S1FULL), 1);
-        mbar_init(bar(L::B_S1FREE), 8);
-        mbar_init(bar(L::B_DPFULL), 1);
-        for (int c = 0; c < L::NCH; ++c) mbar_init(bar(L::B_PFULL + c), 8);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(L::B_SFULL + s), 1);
+            mbar_init(bar(L::B_SFREE + s), L::NDS);
+            mbar_init(bar(L::B_DPFULL + s), 1);
+        }
+        for (int c = 0; c < 2 * L::NCH; ++c) mbar_init(bar(L::B_PFULL + c), L::NDS);
+        for (int s = 0; s < 2; ++s) mbar_init(bar(L::B_GDONE + s), 1);
         mbar_init(bar(L::B_DONE), 1);
         fence_mbar_init();
         prefetch_tensormap(&tm_q1);
@@ -718,112 +765,129 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        // The whole warp runs this loop with warp-uniform values; each MMA and
-        // commit is issued by one elected lane (the *_warp wrappers).
-        {
-            // Every lane waits; a wait that ran out on any lane ends the loop on all.
-            auto wait = [&](uint32_t b, uint32_t parity) -> bool {
-                return __all_sync(0xffffffffu, mbar_wait(b, parity, ERR_SITE_BWD_MMA));
-            };
-            constexpr uint32_t idesc_s = idesc_bf16_f32(L::BK, L::BQ, false);   // S^T, dP^T
-            constexpr uint32_t idesc_dv = idesc_bf16_f32(L::BK, DV, true);      // dV: dO MN-major
-            constexpr uint32_t idesc_dk = idesc_bf16_f32(L::BK, D, true);       // dK: Q MN-major
+    } else if (warp == 1 || warp == L::W_GRAD) {
+        // ------------------------------------------------------------ MMA issuers
+        // Each issuing warp runs its loop with warp-uniform values; each MMA
+        // and commit is issued by one elected lane (the *_warp wrappers).
+        // Every lane waits; a wait that ran out on any lane ends the loop on all.
+        auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(b, parity, ERR_SITE_BWD_MMA));
+        };
+        constexpr uint64_t STAGE16 = L::STAGE >> 4, Q2OFF = L::ST_Q2 >> 4;
+        auto slot_a = [&](int hu) -> uint32_t { return tmem + L::TM_SLOTS + 128u * (uint32_t)hu; };
+        if (warp == 1) {
+            // Scores and dP^T.
+            constexpr uint32_t idesc_s = idesc_bf16_f32(L::BK, L::BU, false);   // S^T, dP^T of one unit
             bool ok = wait(bar(L::B_KV), 0);
             tc_fence_after();
             const uint64_t dk1 = smem_desc(sb + L::OFF_K1, 16, L::QK_SBO, L::QK_SWZ);
             const uint64_t dk2 = smem_desc(sb + L::OFF_K2, 16, L::QK_SBO, L::QK_SWZ);
             const uint64_t dvv = smem_desc(sb + L::OFF_V, 16, 1024, SWZ_128B);
-            const uint64_t dq0 = smem_desc(sb + L::OFF_Q, 16, L::QK_SBO, L::QK_SWZ);              // Q1 (K-major), stage 0
-            const uint64_t dqm0 = smem_desc(sb + L::OFF_Q, L::Q_BYTES, L::QK_SBO, L::QK_SWZ);     // Q1 as MN-major B
-            const uint64_t ddo0 = smem_desc(sb + L::OFF_Q + L::ST_DO, 16, 1024, SWZ_128B);     // dO (K-major)
-            const uint64_t ddom0 = smem_desc(sb + L::OFF_Q + L::ST_DO, L::DO_BOX, 1024, SWZ_128B);   // dO MN-major
-            constexpr uint64_t STAGE16 = L::STAGE >> 4, Q2OFF = L::ST_Q2 >> 4;
-            const uint32_t ta = tmem + L::TM_A, tb = tmem + L::TM_B;
-            // The score products of tile t: S1^T into region A, S2^T into
-            // region B.  They are queued right behind the previous tile's
-            // last gradient products (the MMA pipe runs in issue order, and
-            // those products read both regions), before that tile's stage
-            // is released.
-            auto issue_scores = [&](int t) -> bool {
-                const uint64_t st = (uint64_t)(t % L::QST) * STAGE16;
+            const uint64_t dq0 = smem_desc(sb + L::OFF_Q, 16, L::QK_SBO, L::QK_SWZ);           // Q1 (K-major), stage 0
+            const uint64_t ddo0 = smem_desc(sb + L::OFF_Q + L::ST_DO, 16, 1024, SWZ_128B);   // dO (K-major)
+            constexpr uint64_t QU16 = (L::BU * L::QK_ROW) >> 4, DOU16 = (L::BU * 128) >> 4;   // unit row offsets
+            // S1^T into region A and S2^T into region B of the unit's slot,
+            // once the gradient products of the unit that used it before are
+            // complete.
+            auto issue_scores = [&](int u) -> bool {
+                const int t = u >> 1, hu = u & 1;
+                if (u >= 2 && !wait(bar(L::B_GDONE + hu), (t - 1) & 1)) return false;
                 if (!wait(bar(L::B_QFULL + t % L::QST), (t / L::QST) & 1)) return false;
                 tc_fence_after();
+                const uint64_t q = dq0 + (uint64_t)(t % L::QST) * STAGE16 + (uint64_t)hu * QU16;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    mma_ss_warp(ta, dk1 + (uint64_t)(2 * k), dq0 + st + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
-                mma_commit_warp(bar(L::B_S1FULL));
+                    mma_ss_warp(slot_a(hu), dk1 + (uint64_t)(2 * k), q + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k)
-                    mma_ss_warp(tb, dk2 + (uint64_t)(2 * k), dq0 + st + Q2OFF + (uint64_t)(2 * k), idesc_s,
-                           k > 0 ? 1u : 0u);
+                    mma_ss_warp(slot_a(hu) + 64u, dk2 + (uint64_t)(2 * k), q + Q2OFF + (uint64_t)(2 * k), idesc_s,
+                                k > 0 ? 1u : 0u);
+                mma_commit_warp(bar(L::B_SFULL + hu));
                 return true;
             };
-            if (ok && n_t > 0) ok = issue_scores(0);
-            for (int t = 0; t < n_t && ok; ++t) {
-                const int qs = t % L::QST;
-                const uint64_t st = (uint64_t)qs * STAGE16;
-                // dP^T = V dO^T over S1^T once the dS warps hold it: k over
-                // dv, two 64-column boxes of each operand.
-                ok = wait(bar(L::B_S1FREE), t & 1);
-                if (!ok) break;
+            // dP^T = V dO^T over S1^T once the dS warps hold the slot's
+            // scores: k over dv, two 64-column boxes of each operand.
+            auto issue_dp = [&](int u) -> bool {
+                const int t = u >> 1, hu = u & 1;
+                if (!wait(bar(L::B_SFREE + hu), t & 1)) return false;
                 tc_fence_after();
+                const uint64_t o = ddo0 + (uint64_t)(t % L::QST) * STAGE16 + (uint64_t)hu * DOU16;
 #pragma unroll
                 for (int k = 0; k < DV / 16; ++k)
-                    mma_ss_warp(ta, dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
-                           ddo0 + st + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s,
-                           k > 0 ? 1u : 0u);
-                mma_commit_warp(bar(L::B_DPFULL));
-                // Gradients, chunk by chunk: chunk c is queries
-                // [64 hh + CW c, 64 hh + CW c + CW) of each half hh, CW / 16
-                // k-steps; in bf16 its dS1^T, dS2^T fill the chunk's columns
-                // of region A ([dS1 | dS2], CW / 2 columns each) and
-                // (A1 - lambda A2)^T the first CW / 2 of region B.
+                    mma_ss_warp(slot_a(hu), dvv + (uint64_t)(((k >> 2) * L::V_BOX + (k & 3) * 32) >> 4),
+                                o + (uint64_t)(((k >> 2) * L::DO_BOX + (k & 3) * 32) >> 4), idesc_s, k > 0 ? 1u : 0u);
+                mma_commit_warp(bar(L::B_DPFULL + hu));
+                return true;
+            };
+            if (ok && n_u > 0) ok = issue_scores(0) && issue_scores(1) && issue_dp(0);
+            for (int u = 0; u < n_u && ok; ++u) {
+                if (u + 1 < n_u) ok = issue_dp(u + 1);
+                if (ok && u + 2 < n_u) ok = issue_scores(u + 2);
+            }
+        } else {
+            // Gradient products, chunk by chunk: chunk c of group g is the
+            // unit's queries [GC g + CW c, GC g + CW c + CW), CW / 16 k-steps
+            // (k-step kq: queries [16 kq, 16 kq + 16) of the staged tile).
+            constexpr uint32_t idesc_dv = idesc_bf16_f32(L::BK, DV, true);   // dV: dO MN-major
+            constexpr uint32_t idesc_dk = idesc_bf16_f32(L::BK, D, true);    // dK: Q MN-major
+            const uint64_t dqm0 = smem_desc(sb + L::OFF_Q, L::Q_BYTES, L::QK_SBO, L::QK_SWZ);     // Q1 as MN-major B
+            const uint64_t ddom0 = smem_desc(sb + L::OFF_Q + L::ST_DO, L::DO_BOX, 1024, SWZ_128B);   // dO MN-major
+            bool ok = true;
+            for (int u = 0; u < n_u && ok; ++u) {
+                const int t = u >> 1, hu = u & 1, qs = t % L::QST;
+                const uint64_t st = (uint64_t)qs * STAGE16;
+                // This warp reads the staged Q and dO: observe their copies.
+                ok = wait(bar(L::B_QFULL + qs), (t / L::QST) & 1);
 #pragma unroll
-                for (int c = 0; c < L::NCH; ++c) {
-                    ok = wait(bar(L::B_PFULL + c), t & 1);
+                for (int c = 0; c < L::NCH && ok; ++c) {
+                    ok = wait(bar(L::B_PFULL + hu * L::NCH + c), t & 1);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int g = 0; g < L::NG; ++g) {
 #pragma unroll
                         for (int sub = 0; sub < L::CW / 16; ++sub) {
-                            const int k = (64 * hh + L::CW * c) / 16 + sub;   // queries [16 k, 16 k + 16)
-                            const uint64_t kd = (uint64_t)(k * (16 * 128 >> 4)),
-                                           kq = (uint64_t)(k * (16 * L::QK_ROW >> 4));
-                            const uint32_t acc = (t > 0 || k > 0) ? 1u : 0u;
-                            const uint32_t col = 64u * hh + L::CW * c + 8u * sub;
-                            mma_ts_warp(tmem + L::TM_DV, tb + col, ddom0 + st + kd, idesc_dv, acc);
-                            mma_ts_warp(tmem + L::TM_DK1, ta + col, dqm0 + st + kq, idesc_dk, acc);
-                            mma_ts_warp(tmem + L::TM_DK2, ta + col + L::CW / 2, dqm0 + st + Q2OFF + kq, idesc_dk, acc);
+                            const int kq = (L::BU * hu + L::GC * g + L::CW * c) / 16 + sub;
+                            const uint64_t kd = (uint64_t)(kq * (16 * 128 >> 4)),
+                                           kqq = (uint64_t)(kq * (16 * L::QK_ROW >> 4));
+                            const uint32_t acc = (t > 0 || kq > 0) ? 1u : 0u;
+                            // bf16 operands of k-step sub: 8 columns at 8 sub
+                            // of the chunk's [dS1 | dS2] (CW / 2 columns each)
+                            // and of its (A1 - lambda A2) columns.
+                            const uint32_t col = (uint32_t)(L::GC * g + L::CW * c) + 8u * sub;
+                            mma_ts_warp(tmem + L::TM_DV, slot_a(hu) + 64u + col, ddom0 + st + kd, idesc_dv, acc);
+                            mma_ts_warp(tmem + L::TM_DK1, slot_a(hu) + col, dqm0 + st + kqq, idesc_dk, acc);
+                            mma_ts_warp(tmem + L::TM_DK2, slot_a(hu) + col + L::CW / 2, dqm0 + st + Q2OFF + kqq,
+                                        idesc_dk, acc);
                         }
                     }
                 }
                 if (!ok) break;
-                if (t + 1 < n_t) {
-                    ok = issue_scores(t + 1);
-                    if (!ok) break;
-                }
-                mma_commit_warp(bar(L::B_QEMPTY + qs));
+                mma_commit_warp(bar(L::B_GDONE + hu));
+                // Both units of the staged tile are done with it once these
+                // products complete (the score and dP^T products that read it
+                // completed before the dS warps released these chunks).
+                if (hu == 1) mma_commit_warp(bar(L::B_QEMPTY + qs));
             }
             mma_commit_warp(bar(L::B_DONE));
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ dS (warps 2-9)
-        const int hf = (warp - 2) >> 2;         // half: query columns [64 hf, 64 hf + 64) of each tile
+        // ------------------------------------------------------------ dS (warps 2 .. 2 + NDS - 1)
+        constexpr int GC = L::GC, CW = L::CW;
+        const int grp = (warp - 2) >> 2;        // column group: the unit's query columns [GC grp, GC grp + GC)
         const int wq = warp & 3;                // TMEM lane quarter
         const int row = wq * 32 + lane;         // key row within the tile
         const uint32_t t_lane = (uint32_t)(wq * 32) << 16;
-        const uint32_t ta = tmem + t_lane + L::TM_A + 64u * hf, tb = tmem + t_lane + L::TM_B + 64u * hf;
         const int kj = k0 + row;
         const float sl2 = p.scale_log2;
         const float nlam = -p.lambda;
         bool ok = true;
-        for (int t = 0; t < n_t; ++t) {
-            const int qs = t % L::QST;
-            ok = mbar_wait(bar(L::B_S1FULL), t & 1, ERR_SITE_BWD_SOFTMAX);
+        for (int u = 0; u < n_u; ++u) {
+            const int t = u >> 1, hu = u & 1, qs = t % L::QST;
+            const uint32_t ta = tmem + t_lane + L::TM_SLOTS + 128u * (uint32_t)hu + (uint32_t)(GC * grp);
+            const uint32_t tb = ta + 64u;
+            ok = mbar_wait(bar(L::B_SFULL + hu), t & 1, ERR_SITE_BWD_SOFTMAX);
             // The row constants came in with this stage's copies: observe that
             // barrier too (its phase cannot move on before this tile's PFULL
             // arrivals).
@@ -831,69 +895,59 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            // Row constants of this half's 64 queries, negated: -lse1 log2 e,
+            // Row constants of this group's GC queries, negated: -lse1 log2 e,
             // -lse2 log2 e, -D1, -D2 at rows 0, 128, 256, 384.
-            const float* rct =
-                reinterpret_cast<const float*>(smem + L::OFF_Q + (uint32_t)qs * L::STAGE + L::ST_RC) + 64 * hf;
-            const int qbase = (t0 + t) * L::BQ + 64 * hf;   // query of column 0
+            const float* rct = reinterpret_cast<const float*>(smem + L::OFF_Q + (uint32_t)qs * L::STAGE + L::ST_RC) +
+                               L::BU * hu + GC * grp;
+            const int qbase = (t0 + t) * L::BQ + L::BU * hu + GC * grp;   // query of column 0
             // Causal: key kj is hidden from query qbase + i iff i < lim.  The
             // test runs only in warps that hold a hidden pair (warp-uniform).
             const int lim = kj - qbase - diag;
             const bool wmask = CAUSAL && (k0 + 32 * wq + 31 - qbase - diag > 0);
-            float p1[64];
+            float p1[GC], p2[GC];
             {
-                uint32_t s1[64];
-                tmem_ld64(ta, s1);
-                // S1^T is in registers: its columns may take dP^T.
+                uint32_t s1[GC], s2[GC];
+                tmem_ld32x2(ta, s1, tb, s2);
+                // Both score blocks are in registers: the slot may take dP^T.
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::B_S1FREE));
+                if (lane == 0) mbar_arrive(bar(L::B_SFREE + hu));
 #pragma unroll
-                for (int j = 0; j < 64; j += 4) {
-                    const float4 l = *reinterpret_cast<const float4*>(rct + j);
+                for (int j = 0; j < GC; j += 4) {
+                    const float4 l1 = *reinterpret_cast<const float4*>(rct + j);
+                    const float4 l2 = *reinterpret_cast<const float4*>(rct + 128 + j);
                     float x0, x1, x2, x3;
-                    fma2(x0, x1, __uint_as_float(s1[j]), __uint_as_float(s1[j + 1]), sl2, sl2, l.x, l.y);
-                    fma2(x2, x3, __uint_as_float(s1[j + 2]), __uint_as_float(s1[j + 3]), sl2, sl2, l.z, l.w);
+                    fma2(x0, x1, __uint_as_float(s1[j]), __uint_as_float(s1[j + 1]), sl2, sl2, l1.x, l1.y);
+                    fma2(x2, x3, __uint_as_float(s1[j + 2]), __uint_as_float(s1[j + 3]), sl2, sl2, l1.z, l1.w);
                     p1[j] = fast_exp2(x0);
                     p1[j + 1] = fast_exp2(x1);
                     p1[j + 2] = fast_exp2(x2);
                     p1[j + 3] = fast_exp2(x3);
+                    fma2(x0, x1, __uint_as_float(s2[j]), __uint_as_float(s2[j + 1]), sl2, sl2, l2.x, l2.y);
+                    fma2(x2, x3, __uint_as_float(s2[j + 2]), __uint_as_float(s2[j + 3]), sl2, sl2, l2.z, l2.w);
+                    p2[j] = fast_exp2(x0);
+                    p2[j + 1] = fast_exp2(x1);
+                    p2[j + 2] = fast_exp2(x2);
+                    p2[j + 3] = fast_exp2(x3);
                 }
                 if (wmask) {
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) p1[j] = j < lim ? 0.0f : p1[j];
+                    for (int j = 0; j < GC; ++j) {
+                        p1[j] = j < lim ? 0.0f : p1[j];
+                        p2[j] = j < lim ? 0.0f : p2[j];
+                    }
                 }
             }
-            ok = mbar_wait(bar(L::B_DPFULL), t & 1, ERR_SITE_BWD_SOFTMAX);
+            ok = mbar_wait(bar(L::B_DPFULL + hu), t & 1, ERR_SITE_BWD_SOFTMAX);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
             // NCH chunks of CW queries; the gradient products of chunk c start
             // while chunk c + 1 is computed.
-            constexpr int CW = L::CW;
 #pragma unroll
             for (int c = 0; c < L::NCH; ++c) {
-                uint32_t s2[CW], dp[CW];
-                if constexpr (CW == 16)
-                    tmem_ld16x2(tb + CW * c, s2, ta + CW * c, dp);
-                else
-                    tmem_ld32x2(tb + CW * c, s2, ta + CW * c, dp);
-                float e[CW];
-#pragma unroll
-                for (int j = 0; j < CW; j += 4) {
-                    const float4 l = *reinterpret_cast<const float4*>(rct + 128 + CW * c + j);
-                    float x0, x1, x2, x3;
-                    fma2(x0, x1, __uint_as_float(s2[j]), __uint_as_float(s2[j + 1]), sl2, sl2, l.x, l.y);
-                    fma2(x2, x3, __uint_as_float(s2[j + 2]), __uint_as_float(s2[j + 3]), sl2, sl2, l.z, l.w);
-                    e[j] = fast_exp2(x0);
-                    e[j + 1] = fast_exp2(x1);
-                    e[j + 2] = fast_exp2(x2);
-                    e[j + 3] = fast_exp2(x3);
-                }
-                if (wmask) {
-#pragma unroll
-                    for (int j = 0; j < CW; ++j) e[j] = CW * c + j < lim ? 0.0f : e[j];
-                }
+                uint32_t dp[CW];
+                tmem_ld16(ta + CW * c, dp);
                 uint32_t w1[CW / 2], w2[CW / 2], wd[CW / 2];
 #pragma unroll
                 for (int j = 0; j < CW; j += 4) {
@@ -901,12 +955,12 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                     const float4 n2 = *reinterpret_cast<const float4*>(rct + 384 + CW * c + j);
 #pragma unroll
                     for (int h2 = 0; h2 < 4; h2 += 2) {
-                        const int q = CW * c + j + h2;   // column within the half
+                        const int q = CW * c + j + h2;   // column within the group
                         const float d0 = __uint_as_float(dp[j + h2]), d1 = __uint_as_float(dp[j + h2 + 1]);
                         float u0, u1, v0, v1, g0, g1, a0, a1, b0, b1, c0, c1;
                         add2(u0, u1, d0, d1, h2 ? n1.z : n1.x, h2 ? n1.w : n1.y);   // dP - D1
                         add2(v0, v1, d0, d1, h2 ? n2.z : n2.x, h2 ? n2.w : n2.y);   // dP - D2
-                        mul2(g0, g1, e[j + h2], e[j + h2 + 1], nlam, nlam);        // -lambda A2
+                        mul2(g0, g1, p2[q], p2[q + 1], nlam, nlam);                // -lambda A2
                         mul2(a0, a1, p1[q], p1[q + 1], u0, u1);                    // dS1
                         mul2(b0, b1, g0, g1, v0, v1);                              // dS2
                         add2(c0, c1, p1[q], p1[q + 1], g0, g1);                    // A1 - lambda A2
@@ -915,19 +969,13 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
                         wd[(j + h2) >> 1] = pack_bf16x2(c0, c1);
                     }
                 }
-                if constexpr (CW == 16) {
-                    tmem_st8(ta + CW * c, w1);
-                    tmem_st8(ta + CW * c + CW / 2, w2);
-                    tmem_st8(tb + CW * c, wd);
-                } else {
-                    tmem_st16(ta + CW * c, w1);
-                    tmem_st16(ta + CW * c + CW / 2, w2);
-                    tmem_st16(tb + CW * c, wd);
-                }
+                tmem_st8(ta + CW * c, w1);
+                tmem_st8(ta + CW * c + CW / 2, w2);
+                tmem_st8(tb + CW * c, wd);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::B_PFULL + c));
+                if (lane == 0) mbar_arrive(bar(L::B_PFULL + hu * L::NCH + c));
             }
         }
         // ------------------------------------------------------------ epilogue
@@ -935,41 +983,17 @@ bwd_dkv_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         __syncwarp();
         tc_fence_after();
         const bool store = kj < p.Nk;
-        // dV: columns [dv/2 hf, dv/2 (hf + 1)).
+        // dV: columns [dv/2 grp, dv/2 (grp + 1)); dK1, dK2: columns
+        // [d/2 grp, d/2 (grp + 1)), times 1/sqrt(d).
+        constexpr int VC = DV / L::NG, KC = D / L::NG;
 #pragma unroll
-        for (int c = 0; c < DV / 64; ++c) {
-            uint32_t a[32];
-            tmem_ld32(tmem + t_lane + L::TM_DV + (DV / 2) * hf + 32 * c, a);
-            if (store) {
-                uint4* dst = reinterpret_cast<uint4*>(p.dv + (bh * p.Nk + kj) * DV + (DV / 2) * hf + 32 * c);
+        for (int c = 0; c < VC; c += 32)
+            tmem_cols_to_bf16<32>(tmem + t_lane + L::TM_DV + (uint32_t)(VC * grp + c),
+                                  p.dv + (bh * p.Nk + kj) * DV + VC * grp + c, 1.0f, store);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pack_bf16x2(__uint_as_float(a[8 * i]), __uint_as_float(a[8 * i + 1])),
-                                        pack_bf16x2(__uint_as_float(a[8 * i + 2]), __uint_as_float(a[8 * i + 3])),
-                                        pack_bf16x2(__uint_as_float(a[8 * i + 4]), __uint_as_float(a[8 * i + 5])),
-                                        pack_bf16x2(__uint_as_float(a[8 * i + 6]), __uint_as_float(a[8 * i + 7])));
-            }
-        }
-        // dK1, dK2: columns [d/2 hf, d/2 (hf + 1)), times 1/sqrt(d).
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            uint32_t a[D / 2];
-            if constexpr (D == 64)
-                tmem_ld32(tmem + t_lane + (r ? L::TM_DK2 : L::TM_DK1) + (D / 2) * hf, a);
-            else
-                tmem_ld16(tmem + t_lane + (r ? L::TM_DK2 : L::TM_DK1) + (D / 2) * hf, a);
-            if (store) {
-                uint4* dst = reinterpret_cast<uint4*>((r ? p.dk2 : p.dk1) + (bh * p.Nk + kj) * D + (D / 2) * hf);
-                const float s = p.scale;
-#pragma unroll
-                for (int i = 0; i < D / 16; ++i)
-                    dst[i] = make_uint4(
-                        pack_bf16x2(__uint_as_float(a[8 * i]) * s, __uint_as_float(a[8 * i + 1]) * s),
-                        pack_bf16x2(__uint_as_float(a[8 * i + 2]) * s, __uint_as_float(a[8 * i + 3]) * s),
-                        pack_bf16x2(__uint_as_float(a[8 * i + 4]) * s, __uint_as_float(a[8 * i + 5]) * s),
-                        pack_bf16x2(__uint_as_float(a[8 * i + 6]) * s, __uint_as_float(a[8 * i + 7]) * s));
-            }
-        }
+        for (int r = 0; r < 2; ++r)
+            tmem_cols_to_bf16<KC>(tmem + t_lane + (r ? L::TM_DK2 : L::TM_DK1) + (uint32_t)(KC * grp),
+                                  (r ? p.dk2 : p.dk1) + (bh * p.Nk + kj) * D + KC * grp, p.scale, store);
     }
 
     tc_fence_before();

@@ -118,3 +118,45 @@ def test_decode_32k_every_head():
         worst_out = max(worst_out, float(np.abs(got_out - y_ref).max()))
     print(f"[parity] decode_32k, all {w.B * w.H} heads: pre-norm {worst_pre:.3e}, normalised {worst_out:.3e}")
     assert worst_pre <= TOL_PRE and worst_out <= TOL_OUT
+
+
+def test_decode_merges_on_any_workspace_contents_and_in_every_graph_replay():
+    """The workspace needs no initialisation: whatever bytes it holds, and
+    whatever an earlier call left there, the merge of every (b, h) reads only
+    what this call's split kernel wrote.  A CUDA graph that captured the call
+    reproduces it on every replay.  Outputs are set to NaN before each call
+    and each replay, so a head that is not merged fails the comparison."""
+    B, H, Nk, d, dv, splits = 4, 8, 3000, 64, 128, 5
+    inp = random_cache(B, H, Nk, d, dv, 31, gamma=True)
+    ref_out, ref_pre = gpu_decode(inp, 0.6, 0.8, splits=splits)
+    ws = torch.empty(da.decode_workspace_bytes(B, H, Nk, dv, splits), dtype=torch.uint8, device="cuda")
+    out = torch.empty((B, H, 1, dv), dtype=torch.bfloat16, device="cuda")
+    pre = torch.empty((B, H, 1, dv), dtype=torch.float32, device="cuda")
+    run = lambda: da.decode(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], 0.6, 0.8, gamma=inp["gamma"],
+                            num_splits=splits, workspace=ws, out=out, o_prenorm=pre)
+    g = torch.Generator(device="cuda").manual_seed(32)
+    fills = [lambda: ws.fill_(0xFF), lambda: ws.zero_(), lambda: ws.fill_(0x5A),
+             lambda: ws.copy_(torch.randint(0, 256, ws.shape, generator=g, device="cuda", dtype=torch.uint8))]
+    for fill in fills:
+        fill()
+        out.fill_(float("nan"))
+        pre.fill_(float("nan"))
+        run()
+        run()   # a second call on what the first left in the counters
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out) and torch.equal(pre, ref_pre)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    for _ in range(4):
+        out.fill_(float("nan"))
+        pre.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out) and torch.equal(pre, ref_pre)
+    assert da.last_device_error() == 0

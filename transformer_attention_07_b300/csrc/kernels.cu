@@ -115,6 +115,16 @@ static int sm_count() {
 #endif
 static constexpr int kPersistMaxNk = DIFFATTN_PERSIST_MAX_NK;
 
+// The persistent grids walk their tiles weight-major across all heads (the
+// better balance) under causal masking when every head's K and V together
+// take at most this many bytes, half the B300's 126 MB L2; larger problems
+// walk (b, h)-major so that the tiles in flight share their heads' K and V.
+static constexpr long long kWeightMajorMaxBytes = 64ll << 20;
+
+static int weight_major_order(bool causal, int B, int H, int Nk, long long bytes_per_key) {
+    return causal && (long long)B * H * Nk * bytes_per_key <= kWeightMajorMaxBytes ? 1 : 0;
+}
+
 template <int D, int DV, bool CAUSAL, bool QK8>
 static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     using L = PrefillLayout<D, DV, QK8>;
@@ -145,6 +155,7 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     p.o2 = a.o2;
     p.lse = a.lse;
     p.qk_scale = a.qk_scale;
+    p.weight_major = weight_major_order(CAUSAL, a.B, a.H, a.Nk, 2ll * D * qe + 2ll * DV);
     const long long tiles = (long long)((a.Nq + L::BM - 1) / L::BM) * a.H * a.B;
     const int sms = sm_count();
     const bool persist = sms > 0 && tiles > sms && a.Nk <= kPersistMaxNk;
@@ -296,6 +307,7 @@ static int launch_standard_t(const StandardArgs& a, cudaStream_t st) {
     p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)L::D));
     p.out = static_cast<uint16_t*>(a.out);
     p.out_f32 = a.out_f32;
+    p.weight_major = weight_major_order(CAUSAL, a.B, a.H, a.Nk, 2ll * (L::D + L::DV));
     // Persistent for short sequences, as the differential prefill.
     const long long pairs = (long long)((a.Nq + 2 * L::BM - 1) / (2 * L::BM)) * a.H * a.B;
     const int sms = sm_count();

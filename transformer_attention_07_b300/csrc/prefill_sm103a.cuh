@@ -53,6 +53,7 @@ struct PrefillParams {
     float* o2;              // fp32 [B,H,Nq,dv] or null: A2 V (the second map's normalised output)
     float* lse;             // fp32 [2,B,H,Nq] or null: log sum_j exp(s_r,ij), natural log, per map
     const float* qk_scale;  // [4,H] dequantisation scales of q1, k1, q2, k2 per head (fp8 inputs), or null
+    int weight_major;       // persistent form: order the tiles by weight across all heads (see prefill_kernel)
 };
 
 // QK8: Q1, Q2, K1, K2 are fp8 (e4m3) with per-head scales, and Q K^T runs
@@ -136,8 +137,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
 
     // Tiles: heaviest (right-most under causal masking) query tiles first.
     // Without PERSIST the CTA owns tile (blockIdx.x, y, z); with it, tile
-    // number t = k G + (k even ? c : G - 1 - c) of the (b, h)-major,
-    // heaviest-first order for k = 0, 1, ... (c = blockIdx.x, G = gridDim.x).
+    // number t = k G + (k even ? c : G - 1 - c) for k = 0, 1, ... (c =
+    // blockIdx.x, G = gridDim.x) of one of two orders:
+    //   * (b, h)-major, heaviest first within each (b, h): the CTAs at work at
+    //     any time share a few heads' K and V, which stay in L2;
+    //   * weight-major (p.weight_major), heaviest first across all heads: the
+    //     alternating walk then hands every CTA nearly the same number of key
+    //     tiles (at causal 2K, B4 H8: the busiest CTA 4% above the mean
+    //     instead of 16%), but the CTAs at work span all heads, so the launcher
+    //     takes it only when every head's K and V fit in L2 together.
     const int num_qt = (p.Nq + L::BM - 1) / L::BM;
     const int diag = p.Nk - p.Nq;   // key j visible to query i iff j <= i + diag (causal)
     auto tile = [&](int k, int& qt, int& h, int& b) -> bool {
@@ -149,9 +157,17 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         } else {
             const long long G = gridDim.x, c = blockIdx.x;
             const long long t = (long long)k * G + ((k & 1) ? G - 1 - c : c);
-            if (t >= (long long)num_qt * p.H * p.B) return false;
-            const long long bh = t / num_qt;
-            qt = num_qt - 1 - (int)(t - bh * num_qt);
+            const long long BH = (long long)p.H * p.B;
+            if (t >= (long long)num_qt * BH) return false;
+            long long bh, w;
+            if (p.weight_major) {
+                w = t / BH;
+                bh = t - w * BH;
+            } else {
+                bh = t / num_qt;
+                w = t - bh * num_qt;
+            }
+            qt = num_qt - 1 - (int)w;
             h = (int)(bh % p.H);
             b = (int)(bh / p.H);
             return true;

@@ -37,6 +37,7 @@ struct StandardParams {
     float scale_log2;       // log2(e) / sqrt(d)
     uint16_t* out;          // bf16 [B,H,Nq,dv]
     float* out_f32;         // fp32 [B,H,Nq,dv] or null
+    int weight_major;       // persistent form: order the tile pairs by weight across all heads
 };
 
 struct StandardLayout {
@@ -102,9 +103,17 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         } else {
             const long long G = gridDim.x, c = blockIdx.x;
             const long long t = (long long)k * G + ((k & 1) ? G - 1 - c : c);
-            if (t >= (long long)num_pairs * p.H * p.B) return false;
-            const long long bh = t / num_pairs;
-            pr = num_pairs - 1 - (int)(t - bh * num_pairs);
+            const long long BH = (long long)p.H * p.B;
+            if (t >= (long long)num_pairs * BH) return false;
+            long long bh, w;
+            if (p.weight_major) {   // as in the differential prefill
+                w = t / BH;
+                bh = t - w * BH;
+            } else {
+                bh = t / num_pairs;
+                w = t - bh * num_pairs;
+            }
+            pr = num_pairs - 1 - (int)w;
             h = (int)(bh % p.H);
             b = (int)(bh / p.H);
             return true;

@@ -54,6 +54,7 @@ struct PrefillParams {
     float* lse;             // fp32 [2,B,H,Nq] or null: log sum_j exp(s_r,ij), natural log, per map
     const float* qk_scale;  // [4,H] dequantisation scales of q1, k1, q2, k2 per head (fp8 inputs), or null
     int weight_major;       // persistent form: order the tiles by weight across all heads (see prefill_kernel)
+    int head_group;         // one-tile form, > 0: a 1-D grid in weight order within groups of this many heads
 };
 
 // QK8: Q1, Q2, K1, K2 are fp8 (e4m3) with per-head scales, and Q K^T runs
@@ -146,13 +147,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
     //     tiles (at causal 2K, B4 H8: the busiest CTA 4% above the mean
     //     instead of 16%), but the CTAs at work span all heads, so the launcher
     //     takes it only when every head's K and V fit in L2 together.
+    // The one-tile form under causal masking runs a 1-D grid (p.head_group >
+    // 0): the hardware starts the CTAs in index order, and the index walks
+    // groups of p.head_group heads (as many as fit 16 MB of K and V, when that
+    // is at least four; otherwise the (b, h)-major 3-D grid), heaviest tiles
+    // of the whole group first.  The last CTAs to start are then the
+    // lightest tiles of the last group, not the lightest tiles of each head
+    // behind the heaviest of the next (at causal 8K, B2 H16, the modelled
+    // finish moves from 6.6% above a perfect split to 0.3%).
     const int num_qt = (p.Nq + L::BM - 1) / L::BM;
     const int diag = p.Nk - p.Nq;   // key j visible to query i iff j <= i + diag (causal)
     auto tile = [&](int k, int& qt, int& h, int& b) -> bool {
         if constexpr (!PERSIST) {
-            qt = num_qt - 1 - (int)blockIdx.x;
-            h = blockIdx.y;
-            b = blockIdx.z;
+            if (p.head_group > 0) {
+                const long long BH = (long long)p.H * p.B, HG = p.head_group, t = blockIdx.x;
+                const long long g = t / (HG * num_qt), r = t - g * HG * num_qt;
+                const long long ng = BH - g * HG < HG ? BH - g * HG : HG;   // heads in this group
+                const long long w = r / ng, bh = g * HG + (r - w * ng);
+                qt = num_qt - 1 - (int)w;
+                h = (int)(bh % p.H);
+                b = (int)(bh / p.H);
+            } else {
+                qt = num_qt - 1 - (int)blockIdx.x;
+                h = blockIdx.y;
+                b = blockIdx.z;
+            }
             return k == 0;
         } else {
             const long long G = gridDim.x, c = blockIdx.x;

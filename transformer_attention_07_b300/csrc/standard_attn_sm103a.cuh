@@ -38,6 +38,7 @@ struct StandardParams {
     uint16_t* out;          // bf16 [B,H,Nq,dv]
     float* out_f32;         // fp32 [B,H,Nq,dv] or null
     int weight_major;       // persistent form: order the tile pairs by weight across all heads
+    int head_group;         // one-pair form, > 0: a 1-D grid in weight order within groups of this many heads
 };
 
 struct StandardLayout {
@@ -96,9 +97,19 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int diag = p.Nk - p.Nq;
     auto tile = [&](int k, int& pr, int& h, int& b) -> bool {
         if constexpr (!PERSIST) {
-            pr = num_pairs - 1 - (int)blockIdx.x;
-            h = blockIdx.y;
-            b = blockIdx.z;
+            if (p.head_group > 0) {   // as in the differential prefill
+                const long long BH = (long long)p.H * p.B, HG = p.head_group, t = blockIdx.x;
+                const long long g = t / (HG * num_pairs), r = t - g * HG * num_pairs;
+                const long long ng = BH - g * HG < HG ? BH - g * HG : HG;
+                const long long w = r / ng, bh = g * HG + (r - w * ng);
+                pr = num_pairs - 1 - (int)w;
+                h = (int)(bh % p.H);
+                b = (int)(bh / p.H);
+            } else {
+                pr = num_pairs - 1 - (int)blockIdx.x;
+                h = blockIdx.y;
+                b = blockIdx.z;
+            }
             return k == 0;
         } else {
             const long long G = gridDim.x, c = blockIdx.x;

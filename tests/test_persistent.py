@@ -10,7 +10,15 @@ persistent form.  Two checks per shape:
   * sampled rows (first and last rows, tile boundaries) against the fp64
     oracle within the parity tolerances (1e-2 pre-norm, 3e-2 normalised).
 The shapes cover ragged Nq < Nk, non-causal ragged keys, d = 32, and tile
-counts that end in a partial round after rounds in both directions.
+counts that end in a partial round after rounds in both directions.  Under
+causal masking the tile list is weight-major when every head's K and V fit
+in 64 MB together (the first, third and fourth shapes) and (b, h)-major
+otherwise (the fifth, 335 MB).
+
+The one-tile form under causal masking runs a 1-D grid in weight order
+within groups of heads when at least four heads' K and V fit in 16 MB;
+`test_grouped_one_tile_grid` checks it the same way, each head against a
+call on that head alone (one head: the (b, h, tile) 3-D grid).
 """
 import math
 
@@ -53,6 +61,7 @@ def boundary_rows(Nq):
     (2, 50, 256, 777, 64, 128, False),    # non-causal, ragged keys; 200 tiles
     (3, 50, 640, 640, 64, 128, True),     # 750 tiles: five rounds in alternating directions, then a partial one
     (1, 160, 200, 200, 32, 64, True),     # d = 32, dv = 64; 320 tiles
+    (4, 40, 640, 4096, 64, 128, True),    # 800 tiles, K/V 335 MB: the (b, h)-major list
 ])
 def test_persistent_prefill(B, H, Nq, Nk, d, dv, causal):
     tiles = B * H * math.ceil(Nq / 128)
@@ -110,3 +119,35 @@ def test_persistent_single_map_kernel():
     e32 = np.abs(out32.cpu().numpy()[:, :, rows] - o_ref).max()
     print(f"[parity] persistent single-map max-abs error: {e32:.3e}")
     assert np.isfinite(e32) and e32 <= 1e-2
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk", [
+    (1, 12, 640, 5000),   # 60 tiles, 2.6 MB of K/V per head: groups of 6 heads
+    (2, 5, 300, 6000),    # 30 tiles, 10 heads in groups of 5, ragged rows
+])
+def test_grouped_one_tile_grid(B, H, Nq, Nk):
+    d, dv = 64, 128
+    tiles = B * H * math.ceil(Nq / 128)
+    assert tiles <= sms() or Nk > MAX_PERSIST_NK, "shape would take the persistent form"
+    assert (16 << 20) // (Nk * (2 * d + dv) * 2) >= 4, "fewer than four heads per group"
+    lam, lam_init, eps = 0.6, 0.8, 1e-5
+    inp = random_inputs(B, H, Nq, Nk, d, dv, seed=Nq + Nk + 5 * H)
+    out = da.fwd(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], lam, lam_init, causal=True,
+                 gamma=inp["gamma"], eps=eps)
+    for b in range(B):
+        for h in range(H):
+            one = {k: inp[k][b:b + 1, h:h + 1].contiguous() for k in ("q1", "k1", "q2", "k2", "v")}
+            out1 = da.fwd(one["q1"], one["k1"], one["q2"], one["k2"], one["v"], lam, lam_init, causal=True,
+                          gamma=inp["gamma"][h * dv:(h + 1) * dv].contiguous(), eps=eps)
+            assert torch.equal(out1[0, 0], out[b, h]), (b, h)
+    g = torch.Generator(device="cuda").manual_seed(B * H + Nq)
+    mk = lambda *s: torch.randn(s, generator=g, device="cuda").to(torch.bfloat16)
+    q, k, v = mk(B, H, Nq, 128), mk(B, H, Nk, 128), mk(B, H, Nk, 128)
+    o = da.standard_fwd(q, k, v, causal=True)
+    for b in range(B):
+        for h in range(H):
+            o1 = da.standard_fwd(q[b:b + 1, h:h + 1].contiguous(), k[b:b + 1, h:h + 1].contiguous(),
+                                 v[b:b + 1, h:h + 1].contiguous(), causal=True)
+            assert torch.equal(o1[0, 0], o[b, h]), (b, h)
+    torch.cuda.synchronize()
+    assert da.last_device_error() == 0

@@ -251,14 +251,16 @@ def compare_single_map(dev, reps=10):
     return res
 
 
-def paged_decode_throughput(dev, reps=10):
+def paged_decode_throughput(dev, reps=10, batch=32):
     """Paged split-KV decode on decode_32k-sized caches (B=32, H=32, up to
     32768 keys, d=64, dv=128) in shuffled pages of 64 keys: all sequences
     full, then lengths spread over [1024, 32768].  Algorithmic bytes: the
-    K1, K2 and V rows each sequence owns, read once, plus q and out."""
+    K1, K2 and V rows each sequence owns, read once, plus q and out.  A
+    smaller batch (--paged-batch) gives a case small enough for profiler
+    counters."""
     import torch
     import transformer_attention_07_b300 as da
-    B, H, N, P, d, dv = 32, 32, 32768, 64, 64, 128
+    B, H, N, P, d, dv = batch, 32, 32768, 64, 64, 128
     max_pages = N // P
     gen = torch.Generator(device=dev)
     gen.manual_seed(3000)
@@ -490,7 +492,8 @@ def run_cuda(args, world, rank, local):
         print(json.dumps({"fp8_qk": fp8_throughput(dev, wp, pin, reps=args.steps)}), flush=True)
         return 0
     if args.only == "paged":
-        print(json.dumps({"decode_paged": paged_decode_throughput(dev, reps=args.steps)}), flush=True)
+        print(json.dumps({"decode_paged": paged_decode_throughput(dev, reps=args.steps, batch=args.paged_batch)}),
+              flush=True)
         return 0
     if args.only == "lengths":
         print(json.dumps({"prefill_by_length": prefill_by_length(dev, reps=args.steps)}), flush=True)
@@ -671,6 +674,7 @@ def main():
                     default="all",
                     help="run one stage per step (profiling of a single kernel)")
     ap.add_argument("--prefill-workload", default=PREFILL)
+    ap.add_argument("--paged-batch", type=int, default=32, help="batch of the paged-decode stage (profiling)")
     ap.add_argument("--decode-workload", default=DECODE)
     args = ap.parse_args()
     world, rank, local = dist_setup()

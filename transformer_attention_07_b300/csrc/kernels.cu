@@ -258,7 +258,7 @@ static int launch_backward_t(const BwdArgs& a, cudaStream_t st) {
     if (!cuda_ok(cudaGetLastError(), "backward: prep launch")) return LAUNCH_ERR_CUDA;
 
     CUtensorMap q1a, q2a, doa, k1a, k2a, va;   // dQ sweep: 128-row Q/dO boxes, BN-row K/V boxes
-    CUtensorMap q1b, q2b, dob, k1b, k2b, vb;   // dK/dV sweep: 64-row Q/dO boxes, 128-row K/V boxes
+    CUtensorMap q1b, q2b, dob, k1b, k2b, vb;   // dK/dV sweep: 128-row Q/dO boxes (two 64-query units), 128-row K/V boxes
     const auto S = CU_TENSOR_MAP_SWIZZLE_128B;
     // Q/K rows are one swizzle span wide: 128 bytes (d = 64) or 64 bytes (d = 32).
     const auto SQ = D == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;

@@ -402,4 +402,80 @@ decode_merge_kernel(const MergeParams p) {
     }
 }
 
+// Merge with one CTA per (b, h) and one thread per output column, for heads
+// with at most TMAX partial states: every load of the merge is issued at once
+// (one round of memory latency instead of one per partial), the normaliser
+// and the GroupNorm statistics are block reductions.  Same algebra as
+// merge_head; the per-column output sum runs over the partials in the same
+// order.
+constexpr int kMergeWideMax = 16;
+
+template <int DV>
+__global__ void __launch_bounds__(DV)
+decode_merge_wide_kernel(const MergeParams p) {
+    constexpr int PART = DV + 4, TMAX = kMergeWideMax, NW = DV / 32;
+    __shared__ float red[2][NW];
+    const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
+    const size_t bh = blockIdx.x;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    const int h = (int)(bh % p.H);
+    const size_t BH = (size_t)p.B * p.H;
+    const int T = p.parts * p.S;   // <= TMAX (the launcher's choice)
+    float m[2][TMAX], l[2][TMAX], o[2][TMAX];
+#pragma unroll
+    for (int t = 0; t < TMAX; ++t) {
+        if (t < T) {
+            const int pt = t / p.S, sp = t - pt * p.S;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const float* src = p.ws + ((((size_t)pt * BH + bh) * p.S + sp) * 2 + r) * PART;
+                m[r][t] = __ldcg(src);
+                l[r][t] = __ldcg(src + 1);
+                o[r][t] = __ldcg(src + 4 + c);
+            }
+        }
+    }
+    float O[2], L[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t)
+            if (t < T) M = fmaxf(M, m[r][t]);
+        float Ls = 0.f, Os = 0.f;
+#pragma unroll
+        for (int t = 0; t < TMAX; ++t) {
+            if (t < T && m[r][t] != -INFINITY) {
+                const float e = fast_exp2(m[r][t] - M);
+                Ls = fmaf(l[r][t], e, Ls);
+                Os = fmaf(o[r][t], e, Os);
+            }
+        }
+        O[r] = Os;
+        L[r] = Ls;
+    }
+    const float inv1 = 1.0f / L[0], inv2 = p.lambda / L[1];
+    const float ov = __fmul_rn(O[0], inv1) - __fmul_rn(O[1], inv2);   // no contraction: exact cancel
+    float x = warp_sum(ov);
+    if (lane == 0) red[0][warp] = x;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot += red[0][w];
+    const float mu = tot * (1.0f / DV);
+    x = warp_sum((ov - mu) * (ov - mu));
+    if (lane == 0) red[1][warp] = x;
+    __syncthreads();
+    tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) tot += red[1][w];
+    const float var = tot * (1.0f / DV);
+    const float sc = (1.0f - p.lambda_init) * rsqrtf(var + p.eps);
+    if (p.o_prenorm) p.o_prenorm[bh * DV + c] = ov;
+    const float g = p.gamma ? p.gamma[(size_t)h * DV + c] : 1.0f;
+    const float y = (ov - mu) * sc * g;
+    p.out[bh * DV + c] = (uint16_t)(pack_bf16x2(y, 0.0f) & 0xffffu);
+}
+
 }  // namespace diffattn

@@ -418,8 +418,10 @@ static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
     mp.out = static_cast<uint16_t*>(a.out);
     mp.o_prenorm = a.o_prenorm;
     const int heads = a.B * a.H;
-    return cuda_ok(launch_dependent(decode_merge_kernel<DV>, dim3((heads + 3) / 4), dim3(128), 0, st, mp),
-                   "decode: merge launch")
+    const cudaError_t e = mp.parts * mp.S <= kMergeWideMax
+                              ? launch_dependent(decode_merge_wide_kernel<DV>, dim3(heads), dim3(DV), 0, st, mp)
+                              : launch_dependent(decode_merge_kernel<DV>, dim3((heads + 3) / 4), dim3(128), 0, st, mp);
+    return cuda_ok(e, "decode: merge launch")
                ? LAUNCH_OK
                : LAUNCH_ERR_CUDA;
 }
@@ -439,10 +441,13 @@ int launch_decode_merge(const MergeArgs& a, cudaStream_t st) {
     mp.o_prenorm = a.o_prenorm;
     const int heads = a.B * a.H;
     cudaError_t e;
+    const bool wide = a.parts * a.splits <= kMergeWideMax;
     if (a.dv == 128)
-        e = launch_dependent(decode_merge_kernel<128>, dim3((heads + 3) / 4), dim3(128), 0, st, mp);
+        e = wide ? launch_dependent(decode_merge_wide_kernel<128>, dim3(heads), dim3(128), 0, st, mp)
+                 : launch_dependent(decode_merge_kernel<128>, dim3((heads + 3) / 4), dim3(128), 0, st, mp);
     else if (a.dv == 64)
-        e = launch_dependent(decode_merge_kernel<64>, dim3((heads + 3) / 4), dim3(128), 0, st, mp);
+        e = wide ? launch_dependent(decode_merge_wide_kernel<64>, dim3(heads), dim3(64), 0, st, mp)
+                 : launch_dependent(decode_merge_kernel<64>, dim3((heads + 3) / 4), dim3(128), 0, st, mp);
     else
         return LAUNCH_ERR_UNSUPPORTED;
     return cuda_ok(e, "decode: merge of gathered partials") ? LAUNCH_OK : LAUNCH_ERR_CUDA;

@@ -318,8 +318,8 @@ def decode(q1, k1, q2, k2, v, lam, lam_init, gamma=None, eps=1e-5, num_splits=0,
     if Nq != 1:
         raise ValueError("decode takes one query per (b, h)")
     Nk, dv = k1.shape[2], v.shape[3]
-    nbytes = decode_workspace_bytes(B, H, Nk, dv, num_splits)
-    if workspace is None:
+    if workspace is None:   # (a given workspace is size-checked by the library)
+        nbytes = decode_workspace_bytes(B, H, Nk, dv, num_splits)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q1.device)
     if out is None:
         out = torch.empty((B, H, 1, dv), dtype=torch.bfloat16, device=q1.device)

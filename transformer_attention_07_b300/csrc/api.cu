@@ -99,14 +99,8 @@ int choose_splits(int64_t heads, int Nk, int bytes_per_key, int sms, int max_spl
 
 int key_bytes(int d, int dv) { return (2 * d + dv) * 2; }
 
-// Streaming multiprocessors of the current device, or 0 if the runtime cannot say.
-int device_sms() {
-    int dev = 0, sms = 0;
-    if (!diffattn::cuda_ok(cudaGetDevice(&dev), "decode: get device") ||
-        !diffattn::cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev), "decode: SM count"))
-        return 0;
-    return sms;
-}
+// Streaming multiprocessors of the current device (cached per device), or 0.
+int device_sms() { return diffattn::sm_count(); }
 
 // Argument checks of the contiguous-cache decode entry points (everything
 // but the workspace); DIFFATTN_OK when the call may proceed.
@@ -376,12 +370,8 @@ int diffattn_decode_paged(const void* q1, const void* q2, const void* k1_pages, 
     };
     int splits = num_splits;
     if (splits == 0) {
-        int dev = 0, sms = 0;
-        if (!diffattn::cuda_ok(cudaGetDevice(&dev), "paged decode: get device") ||
-            !diffattn::cuda_ok(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
-                               "paged decode: SM count") ||
-            sms < 1)
-            return DIFFATTN_ERR_CUDA;
+        const int sms = device_sms();
+        if (sms < 1) return DIFFATTN_ERR_CUDA;
         splits = choose_splits((int64_t)B * H, max_len, key_bytes(d, dv), sms);
         while (!pages_ok(splits) && splits < kMaxSplits) ++splits;
     }

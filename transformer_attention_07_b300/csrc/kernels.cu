@@ -92,7 +92,7 @@ static bool make_map_bhnd(CUtensorMap* m, const void* base, int B, int H, int N,
 
 // Streaming multiprocessors of the current device (0 if unknown), cached per
 // device; safe to call from several host threads.
-static int sm_count() {
+int sm_count() {
     constexpr int kMaxDevices = 64;
     static std::atomic<int> cache[kMaxDevices] = {};
     int dev = 0;

@@ -93,6 +93,10 @@ int launch_selftest_wait(cudaStream_t st);
 // Capacity of the library-owned decode scratch (diffattn_decode_noalloc).
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 
+// Streaming multiprocessors of the current device, looked up once per device
+// and cached; 0 if the runtime cannot say.
+int sm_count();
+
 // Device address and size of that scratch on the current device (looked up
 // on the first call per device).
 int decode_noalloc_scratch(void** ptr, size_t* bytes);

@@ -143,7 +143,7 @@ static int head_group_size(int B, int H, int Nk, long long bytes_per_key) {
 template <int D, int DV, bool CAUSAL, bool QK8>
 static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     using L = PrefillLayout<D, DV, QK8>;
-    CUtensorMap mq1, mq2, mk1, mk2, mv;
+    CUtensorMap mq1, mq2, mk1, mk2, mv, mo;
     // Q/K rows are one swizzle span wide (128, 64 or 32 bytes).
     const CUtensorMapSwizzle qk_swz = L::QK_ROW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                       : L::QK_ROW == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
@@ -153,7 +153,9 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
         !make_map_bhnd(&mq2, a.q2, a.B, a.H, a.Nq, D, D, L::BM, qk_swz, qe) ||
         !make_map_bhnd(&mk1, a.k1, a.B, a.H, a.Nk, D, D, L::BN, qk_swz, qe) ||
         !make_map_bhnd(&mk2, a.k2, a.B, a.H, a.Nk, D, D, L::BN, qk_swz, qe) ||
-        !make_map_bhnd(&mv, a.v, a.B, a.H, a.Nk, DV, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map_bhnd(&mv, a.v, a.B, a.H, a.Nk, DV, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        // output boxes of the persistent form's TMA stores: 32 rows x 64 columns
+        !make_map_bhnd(&mo, a.out, a.B, a.H, a.Nq, DV, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return LAUNCH_ERR_CUDA;
     PrefillParams p;
     p.B = a.B;
@@ -183,7 +185,7 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     const dim3 grid = persist          ? dim3(sms, 1, 1)
                       : p.head_group ? dim3((unsigned)tiles, 1, 1)
                                      : dim3((a.Nq + L::BM - 1) / L::BM, a.H, a.B);
-    kern<<<grid, L::THREADS, smem, st>>>(mq1, mq2, mk1, mk2, mv, p);
+    kern<<<grid, L::THREADS, smem, st>>>(mq1, mq2, mk1, mk2, mv, mo, p);
     return cuda_ok(cudaGetLastError(), "prefill: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }
 
@@ -312,10 +314,12 @@ int launch_backward(const BwdArgs& a, cudaStream_t st) {
 template <bool CAUSAL>
 static int launch_standard_t(const StandardArgs& a, cudaStream_t st) {
     using L = StandardLayout;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_map_bhnd(&mq, a.q, a.B, a.H, a.Nq, L::D, 64, L::BM, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map_bhnd(&mk, a.k, a.B, a.H, a.Nk, L::D, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map_bhnd(&mv, a.v, a.B, a.H, a.Nk, L::DV, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B))
+        !make_map_bhnd(&mv, a.v, a.B, a.H, a.Nk, L::DV, 64, L::BN, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        // output boxes of the persistent form's TMA stores: 32 rows x 64 columns
+        !make_map_bhnd(&mo, a.out, a.B, a.H, a.Nq, L::DV, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B))
         return LAUNCH_ERR_CUDA;
     StandardParams p;
     p.B = a.B;
@@ -338,7 +342,7 @@ static int launch_standard_t(const StandardArgs& a, cudaStream_t st) {
     const dim3 grid = persist          ? dim3(sms, 1, 1)
                       : p.head_group ? dim3((unsigned)pairs, 1, 1)
                                      : dim3((a.Nq + 2 * L::BM - 1) / (2 * L::BM), a.H, a.B);
-    kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq, mk, mv, p);
+    kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq, mk, mv, mo, p);
     return cuda_ok(cudaGetLastError(), "standard attention: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
 }
 

@@ -33,7 +33,10 @@
 //                GroupNorm statistics over dv, gain, (1 - lambda_init), bf16
 //                store (and the optional fp32 pre-norm copy; for training,
 //                also each map's log-sum-exp and A2 V, which the backward
-//                pass reads).
+//                pass reads).  The persistent form at dv = 128 stages each
+//                warp's 32-row x 64-column share of the bf16 output in
+//                shared memory and writes it with one TMA store, so the
+//                next tile's softmax does not queue behind per-row stores.
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   [0,128) S1 (P1 aliases its first 64 columns)   [128,256) S2 / P2
 //   [256,256+dv) O1                                [256+dv,256+2dv) O2
@@ -65,7 +68,12 @@ template <int D, int DV, bool QK8 = false, bool PERSIST = false>
 struct PrefillLayout {
     static constexpr int BM = 128;   // query rows per tile (MMA M)
     static constexpr int BN = 128;   // keys per tile (MMA N of QK^T, K of PV)
-    static constexpr int KST = 3;    // K1/K2 ring depth
+    // Persistent form at dv = 128: the bf16 output leaves through shared
+    // memory by TMA stores (one 32-row x 64-column box per softmax warp,
+    // 128-byte swizzle), so the epilogue's stores do not occupy the
+    // load/store unit.  Its 32 KB of staging take one K stage.
+    static constexpr bool OST = PERSIST && DV == 128;
+    static constexpr int KST = OST ? 2 : 3;    // K1/K2 ring depth
     // V ring depth.  A V tile can be loaded only once the P V product two
     // (three) tiles back has completed, and from L2 under full load it takes
     // about as long as one key tile's work to arrive, so a third stage keeps
@@ -87,7 +95,11 @@ struct PrefillLayout {
     // CTA they lie over Q1, which nothing reads once the epilogue may start.
     static constexpr uint32_t EPI_BYTES = 6 * BM * 4;
     static_assert(EPI_BYTES <= Q_BYTES, "epilogue slots");
-    static constexpr uint32_t OFF_EPI = PERSIST ? OFF_V + VST * V_BYTES : OFF_Q1;
+    static constexpr uint32_t OST_WARP = 32 * 128;   // one warp's staging: 32 rows x 128 bytes
+    static constexpr uint32_t OFF_OST = OFF_V + VST * V_BYTES;   // 1024-byte aligned (swizzle atoms)
+    static constexpr uint32_t OST_BYTES = OST ? 8 * OST_WARP : 0;
+    static_assert(OFF_OST % 1024 == 0, "staging alignment");
+    static constexpr uint32_t OFF_EPI = PERSIST ? OFF_OST + OST_BYTES : OFF_Q1;
     static constexpr uint32_t OFF_BAR = PERSIST ? OFF_EPI + EPI_BYTES : OFF_V + VST * V_BYTES;
     // barrier indices
     static constexpr int B_Q = 0;
@@ -126,7 +138,8 @@ template <int D, int DV, bool CAUSAL, bool QK8 = false, bool PERSIST = false>
 __global__ void __launch_bounds__(384, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
                const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
-               const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+               const PrefillParams p) {
     using L = PrefillLayout<D, DV, QK8, PERSIST>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived from the __shared__ array by pointer
@@ -224,6 +237,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         prefetch_tensormap(&tm_k1);
         prefetch_tensormap(&tm_k2);
         prefetch_tensormap(&tm_v);
+        if constexpr (L::OST) prefetch_tensormap(&tm_out);
     }
     if (warp == 1) {
         tmem_alloc(sb + L::OFF_TMEM_SLOT, L::TMEM_COLS);
@@ -590,7 +604,37 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         named_barrier_sync(1, 256);
         const float var = (epi[4 * L::BM + row] + epi[5 * L::BM + row]) * (1.0f / DV);
         const float sc = (1.0f - p.lambda_init) * rsqrtf(var + p.eps);
-        if (qi < p.Nq) {
+        if constexpr (L::OST) {
+            // Row `row` of this warp's 32 x 64 box: 16-byte chunk i at chunk
+            // position i ^ (row & 7) (the 128-byte swizzle).  Rows at or past
+            // Nq are staged too; the TMA store does not write them.
+            if (p.o_prenorm && qi < p.Nq) {
+                float4* dst = reinterpret_cast<float4*>(p.o_prenorm + rowoff);
+#pragma unroll
+                for (int i = 0; i < HALF / 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
+            const float* __restrict__ g = p.gamma ? p.gamma + (size_t)h * DV + c0 : nullptr;
+            const uint32_t box = L::OFF_OST + (uint32_t)(r * 4 + wq) * L::OST_WARP;
+            // The previous tile's store from this buffer must have read it.
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            uint8_t* srow = smem + box + (uint32_t)lane * 128u;
+#pragma unroll
+            for (int i = 0; i < HALF / 8; ++i) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = (o[8 * i + e] - mu) * sc * (g ? __ldg(g + 8 * i + e) : 1.0f);
+                *reinterpret_cast<uint4*>(srow + (((uint32_t)i ^ (uint32_t)(lane & 7)) << 4)) =
+                    make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                               pack_bf16x2(y[6], y[7]));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_4d(&tm_out, sb + box, c0, qt * L::BM + wq * 32, h, b);
+                bulk_commit_group();
+            }
+        } else if (qi < p.Nq) {
             if (p.o_prenorm) {
                 float4* dst = reinterpret_cast<float4*>(p.o_prenorm + rowoff);
 #pragma unroll
@@ -609,6 +653,9 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         }
         if constexpr (!PERSIST) break;
         }   // query tiles
+        // Leave with no TMA store reading shared memory or still writing.
+        if constexpr (L::OST)
+            if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();

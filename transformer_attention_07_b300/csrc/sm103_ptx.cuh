@@ -110,7 +110,31 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
-// Fetch the 128-byte line holding `p` into L1 (no register result).
+// Tiled bulk store shared -> global of the box of `map` at coordinates (c0,
+// c1, c2, c3); elements outside the tensor are not written.  Tracked by the
+// issuing thread's bulk async-group (bulk_commit_group / bulk_wait_*).  The
+// shared source must be made visible to the async proxy first
+// (fence_proxy_async_smem by every thread that wrote it, then a barrier).
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every bulk group this thread committed has finished reading its
+// shared-memory source (the buffer may then be rewritten).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until every bulk group this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Order this thread's earlier generic-proxy shared-memory writes before later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Programmatic dependent launch.  A grid launched with programmatic stream
 // serialisation may be scheduled before the previous grid on its stream has
 // ended.  grid_dependency_wait() returns once every prerequisite grid has
@@ -123,6 +147,7 @@ __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepco
 
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// Fetch the 128-byte line holding `p` into L1 (no register result).
 __device__ __forceinline__ void prefetch_l1(const void* p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }

@@ -24,7 +24,9 @@
 //                swizzle atoms).
 //   warps 4-7    softmax of query tile 0; warps 8-11 of query tile 1; one
 //                thread per row; the same online softmax as the
-//                differential kernel; epilogue out = O_r / l_r, bf16.
+//                differential kernel; epilogue out = O_r / l_r, bf16
+//                (in the persistent form through shared memory and TMA
+//                stores, as in the differential kernel).
 // Tensor memory: [0,128) S0 / P0, [128,256) S1 / P1, [256,384) O0, [384,512) O1.
 #pragma once
 
@@ -54,7 +56,13 @@ struct StandardLayout {
     static constexpr uint32_t OFF_Q = 0;              // tile r at r * Q_BYTES
     static constexpr uint32_t OFF_K = 2 * Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + KST * K_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_V + VST * V_BYTES;
+    // Persistent form: the bf16 output leaves through shared memory by TMA
+    // stores, one 32-row x 64-column box (128-byte swizzle) per softmax warp
+    // at a time, two per row block.
+    static constexpr uint32_t OST_WARP = 32 * 128;
+    static constexpr uint32_t OFF_OST = OFF_V + VST * V_BYTES;   // 1024-byte aligned
+    static_assert(OFF_OST % 1024 == 0, "staging alignment");
+    static constexpr uint32_t OFF_BAR = OFF_OST + 8 * OST_WARP;
     static constexpr int B_Q = 0;
     static constexpr int B_KFULL = 1;
     static constexpr int B_KEMPTY = B_KFULL + KST;
@@ -79,7 +87,8 @@ struct StandardLayout {
 template <bool CAUSAL, bool PERSIST = false>
 __global__ void __launch_bounds__(384, 1)
 standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_v, const StandardParams p) {
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+                     const StandardParams p) {
     using L = StandardLayout;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, derived from the __shared__ array by pointer
@@ -160,6 +169,7 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         prefetch_tensormap(&tm_q);
         prefetch_tensormap(&tm_k);
         prefetch_tensormap(&tm_v);
+        if constexpr (PERSIST) prefetch_tensormap(&tm_out);
     }
     if (warp == 1) {
         tmem_alloc(sb + L::OFF_TMEM_SLOT, L::TMEM_COLS);
@@ -404,34 +414,79 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_after();
         const float inv = 1.0f / l;
-#pragma unroll
-        for (int c = 0; c < L::DV / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tmem + t_lane + o_col + 32u * c, ov);
-            if (qi < p.Nq) {
-                const size_t off = (((size_t)b * p.H + h) * p.Nq + qi) * L::DV + 32 * c;
-                float o[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(ov[i]) * inv;
-                if (p.out_f32) {
-                    float4* dst = reinterpret_cast<float4*>(p.out_f32 + off);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(p.out + off);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    dst[i] = make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
-                                        pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7]));
-            }
-        }
         if constexpr (PERSIST) {
-            // O has been read: the next pair's products may overwrite it.
-            tc_fence_before();
-            mbar_arrive(bar(L::B_OFREE));
+            // Two 64-column halves through this warp's staging box: row `row`
+            // puts 16-byte chunk i at chunk position i ^ (row & 7).  Rows at
+            // or past Nq are staged too; the TMA store does not write them.
+            const uint32_t box = L::OFF_OST + (uint32_t)(r * 4 + wq) * L::OST_WARP;
+            uint8_t* srow = smem + box + (uint32_t)lane * 128u;
+            const size_t rowoff = (((size_t)b * p.H + h) * p.Nq + qi) * L::DV;
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ov[32];
+                    tmem_ld32(tmem + t_lane + o_col + 64u * c2 + 32u * c, ov);
+                    float o[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(ov[i]) * inv;
+                    if (p.out_f32 && qi < p.Nq) {
+                        float4* dst = reinterpret_cast<float4*>(p.out_f32 + rowoff + 64 * c2 + 32 * c);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[16 * c + i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+                }
+                if (c2 == 1) {
+                    // O has been read: the next pair's products may overwrite it.
+                    tc_fence_before();
+                    mbar_arrive(bar(L::B_OFREE));
+                }
+                // The previous store from this buffer must have read it.
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    *reinterpret_cast<uint4*>(srow + (((uint32_t)i ^ (uint32_t)(lane & 7)) << 4)) =
+                        make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_4d(&tm_out, sb + box, 64 * c2, pr * 2 * L::BM + r * L::BM + wq * 32, h, b);
+                    bulk_commit_group();
+                }
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < L::DV / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(tmem + t_lane + o_col + 32u * c, ov);
+                if (qi < p.Nq) {
+                    const size_t off = (((size_t)b * p.H + h) * p.Nq + qi) * L::DV + 32 * c;
+                    float o[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = __uint_as_float(ov[i]) * inv;
+                    if (p.out_f32) {
+                        float4* dst = reinterpret_cast<float4*>(p.out_f32 + off);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(p.out + off);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pack_bf16x2(o[8 * i], o[8 * i + 1]), pack_bf16x2(o[8 * i + 2], o[8 * i + 3]),
+                                            pack_bf16x2(o[8 * i + 4], o[8 * i + 5]), pack_bf16x2(o[8 * i + 6], o[8 * i + 7]));
+                }
+            }
         }
         if constexpr (!PERSIST) break;
         }   // tile pairs
+        // Leave with no TMA store reading shared memory or still writing.
+        if constexpr (PERSIST)
+            if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before();

@@ -133,6 +133,20 @@ static int weight_major_order(bool causal, int B, int H, int Nk, long long bytes
 // (16 MB) gain 2.3% at causal 8K, B2 H16.
 static constexpr long long kHeadGroupBytes = 16ll << 20;
 
+// The 1-D tile orders (persistent list, grouped one-tile grid) compute tile
+// indices in 32-bit arithmetic; larger problems take the 3-D grid.
+static constexpr long long kMaxTiles1D = 1ll << 30;
+
+// Multiplier and shift of div_inv for divisor d >= 1 (quotients exact for
+// dividends below 2^31).
+static void inv_div(unsigned d, unsigned& m, int& s) {
+    if (d == 0) d = 1;   // empty problems: never used
+    int l = 0;
+    while ((1ull << l) < d) ++l;
+    s = 31 + l;
+    m = (unsigned)(((1ull << s) + d - 1) / d);
+}
+
 static int head_group_size(int B, int H, int Nk, long long bytes_per_key) {
     const long long per_head = (long long)Nk * bytes_per_key;
     long long g = per_head > 0 ? kHeadGroupBytes / per_head : 0;
@@ -175,8 +189,13 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     p.weight_major = weight_major_order(CAUSAL, a.B, a.H, a.Nk, 2ll * D * qe + 2ll * DV);
     const long long tiles = (long long)((a.Nq + L::BM - 1) / L::BM) * a.H * a.B;
     const int sms = sm_count();
-    const bool persist = sms > 0 && tiles > sms && a.Nk <= kPersistMaxNk;
-    p.head_group = CAUSAL && !persist ? head_group_size(a.B, a.H, a.Nk, 2ll * D * qe + 2ll * DV) : 0;
+    // Both 1-D orders index their tiles with 32-bit arithmetic.
+    const bool small = tiles < kMaxTiles1D;
+    const bool persist = sms > 0 && tiles > sms && a.Nk <= kPersistMaxNk && small;
+    inv_div(p.weight_major ? (unsigned)((long long)a.H * a.B) : (unsigned)((a.Nq + L::BM - 1) / L::BM), p.div_major_m,
+            p.div_major_s);
+    inv_div((unsigned)a.H, p.div_h_m, p.div_h_s);
+    p.head_group = CAUSAL && !persist && small ? head_group_size(a.B, a.H, a.Nk, 2ll * D * qe + 2ll * DV) : 0;
     auto kern = persist ? prefill_kernel<D, DV, CAUSAL, QK8, true> : prefill_kernel<D, DV, CAUSAL, QK8, false>;
     const int smem = (int)(persist ? PrefillLayout<D, DV, QK8, true>::SMEM_BYTES : L::SMEM_BYTES);
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),
@@ -333,8 +352,12 @@ static int launch_standard_t(const StandardArgs& a, cudaStream_t st) {
     // Persistent for short sequences, as the differential prefill.
     const long long pairs = (long long)((a.Nq + 2 * L::BM - 1) / (2 * L::BM)) * a.H * a.B;
     const int sms = sm_count();
-    const bool persist = sms > 0 && pairs > sms && a.Nk <= kPersistMaxNk;
-    p.head_group = CAUSAL && !persist ? head_group_size(a.B, a.H, a.Nk, 2ll * (L::D + L::DV)) : 0;
+    const bool small = pairs < kMaxTiles1D;
+    const bool persist = sms > 0 && pairs > sms && a.Nk <= kPersistMaxNk && small;
+    inv_div(p.weight_major ? (unsigned)((long long)a.H * a.B) : (unsigned)((a.Nq + 2 * L::BM - 1) / (2 * L::BM)),
+            p.div_major_m, p.div_major_s);
+    inv_div((unsigned)a.H, p.div_h_m, p.div_h_s);
+    p.head_group = CAUSAL && !persist && small ? head_group_size(a.B, a.H, a.Nk, 2ll * (L::D + L::DV)) : 0;
     auto kern = persist ? standard_attn_kernel<CAUSAL, true> : standard_attn_kernel<CAUSAL, false>;
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::SMEM_BYTES),
                  "standard attention: set shared memory"))

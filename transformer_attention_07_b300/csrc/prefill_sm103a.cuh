@@ -58,6 +58,11 @@ struct PrefillParams {
     const float* qk_scale;  // [4,H] dequantisation scales of q1, k1, q2, k2 per head (fp8 inputs), or null
     int weight_major;       // persistent form: order the tiles by weight across all heads (see prefill_kernel)
     int head_group;         // one-tile form, > 0: a 1-D grid in weight order within groups of this many heads
+    // Persistent form: tile numbers are divided by the major extent (heads
+    // B H in weight-major order, else the query tiles of a head) and head
+    // numbers by H through div_inv with these multipliers and shifts.
+    unsigned div_major_m, div_h_m;
+    int div_major_s, div_h_s;
 };
 
 // QK8: Q1, Q2, K1, K2 are fp8 (e4m3) with per-head scales, and Q K^T runs
@@ -173,13 +178,15 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
     auto tile = [&](int k, int& qt, int& h, int& b) -> bool {
         if constexpr (!PERSIST) {
             if (p.head_group > 0) {
-                const long long BH = (long long)p.H * p.B, HG = p.head_group, t = blockIdx.x;
-                const long long g = t / (HG * num_qt), r = t - g * HG * num_qt;
-                const long long ng = BH - g * HG < HG ? BH - g * HG : HG;   // heads in this group
-                const long long w = r / ng, bh = g * HG + (r - w * ng);
+                const unsigned BH = (unsigned)p.H * (unsigned)p.B, HG = p.head_group, t = blockIdx.x;
+                const unsigned NT = (unsigned)num_qt;
+                const unsigned g = t / (HG * NT), r = t - g * HG * NT;
+                const unsigned ng = BH - g * HG < HG ? BH - g * HG : HG;   // heads in this group
+                const unsigned w = r / ng, bh = g * HG + (r - w * ng);
                 qt = num_qt - 1 - (int)w;
-                h = (int)(bh % p.H);
-                b = (int)(bh / p.H);
+                const unsigned bb = bh / (unsigned)p.H;
+                h = (int)(bh - bb * (unsigned)p.H);
+                b = (int)bb;
             } else {
                 qt = num_qt - 1 - (int)blockIdx.x;
                 h = blockIdx.y;
@@ -187,21 +194,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             }
             return k == 0;
         } else {
-            const long long G = gridDim.x, c = blockIdx.x;
-            const long long t = (long long)k * G + ((k & 1) ? G - 1 - c : c);
-            const long long BH = (long long)p.H * p.B;
-            if (t >= (long long)num_qt * BH) return false;
-            long long bh, w;
+            // 32-bit index arithmetic (the launcher keeps the tile count
+            // below 2^30) with divisions by invariant multipliers: the
+            // softmax warps compute the next tile's indices between two
+            // tiles, where a division's latency delays the next scores.
+            const unsigned G = gridDim.x, c = blockIdx.x;
+            const unsigned t = (unsigned)k * G + ((k & 1) ? G - 1 - c : c);
+            const unsigned BH = (unsigned)p.H * (unsigned)p.B, NT = (unsigned)num_qt;
+            if (t >= NT * BH) return false;
+            unsigned bh, w;
             if (p.weight_major) {
-                w = t / BH;
+                w = div_inv(t, p.div_major_m, p.div_major_s);
                 bh = t - w * BH;
             } else {
-                bh = t / num_qt;
-                w = t - bh * num_qt;
+                bh = div_inv(t, p.div_major_m, p.div_major_s);
+                w = t - bh * NT;
             }
             qt = num_qt - 1 - (int)w;
-            h = (int)(bh % p.H);
-            b = (int)(bh / p.H);
+            const unsigned bb = div_inv(bh, p.div_h_m, p.div_h_s);
+            h = (int)(bh - bb * (unsigned)p.H);
+            b = (int)bb;
             return true;
         }
     };
@@ -437,7 +449,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
         bool ok = true;
         int g = 0;   // key tiles of earlier query tiles (barrier phase counter)
         int qt, h, b;
-        for (int k = 0; ok && tile(k, qt, h, b); ++k) {
+        bool more = tile(0, qt, h, b);
+        for (int k = 0; ok && more; ++k) {
         const int n_kv = kv_tiles(qt);
         const int qi = qt * L::BM + row;
         const int kmax = CAUSAL ? min(qi + diag, p.Nk - 1) : p.Nk - 1;   // last visible key
@@ -652,6 +665,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant_
             }
         }
         if constexpr (!PERSIST) break;
+        more = tile(k + 1, qt, h, b);
         }   // query tiles
         // Leave with no TMA store reading shared memory or still writing.
         if constexpr (L::OST)

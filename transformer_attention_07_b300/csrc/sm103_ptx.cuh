@@ -452,6 +452,15 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
 #undef DA_W8
 
 // max(a, b, c) in one instruction (three-input form of max.f32).
+// floor(n / d) for 0 <= n < 2^31 as (n m) >> s, with s = 31 + ceil(log2 d)
+// and m = ceil(2^s / d) < 2^32 chosen on the host: then 0 <= m d - 2^s < d
+// <= 2^(s - 31), and by Granlund and Montgomery ("Division by invariant
+// integers using multiplication", 1994, Theorem 4.2) the quotient is exact
+// for every n below 2^31.  A few integer instructions instead of a division.
+__device__ __forceinline__ unsigned div_inv(unsigned n, unsigned m, int s) {
+    return (unsigned)(((unsigned long long)n * m) >> s);
+}
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));

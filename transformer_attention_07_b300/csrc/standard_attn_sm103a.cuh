@@ -41,6 +41,11 @@ struct StandardParams {
     float* out_f32;         // fp32 [B,H,Nq,dv] or null
     int weight_major;       // persistent form: order the tile pairs by weight across all heads
     int head_group;         // one-pair form, > 0: a 1-D grid in weight order within groups of this many heads
+    // Persistent form: tile numbers are divided by the major extent (heads
+    // B H in weight-major order, else the query tiles of a head) and head
+    // numbers by H through div_inv with these multipliers and shifts.
+    unsigned div_major_m, div_h_m;
+    int div_major_s, div_h_s;
 };
 
 struct StandardLayout {
@@ -107,13 +112,15 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     auto tile = [&](int k, int& pr, int& h, int& b) -> bool {
         if constexpr (!PERSIST) {
             if (p.head_group > 0) {   // as in the differential prefill
-                const long long BH = (long long)p.H * p.B, HG = p.head_group, t = blockIdx.x;
-                const long long g = t / (HG * num_pairs), r = t - g * HG * num_pairs;
-                const long long ng = BH - g * HG < HG ? BH - g * HG : HG;
-                const long long w = r / ng, bh = g * HG + (r - w * ng);
+                const unsigned BH = (unsigned)p.H * (unsigned)p.B, HG = p.head_group, t = blockIdx.x;
+                const unsigned NT = (unsigned)num_pairs;
+                const unsigned g = t / (HG * NT), r = t - g * HG * NT;
+                const unsigned ng = BH - g * HG < HG ? BH - g * HG : HG;
+                const unsigned w = r / ng, bh = g * HG + (r - w * ng);
                 pr = num_pairs - 1 - (int)w;
-                h = (int)(bh % p.H);
-                b = (int)(bh / p.H);
+                const unsigned bb = bh / (unsigned)p.H;
+                h = (int)(bh - bb * (unsigned)p.H);
+                b = (int)bb;
             } else {
                 pr = num_pairs - 1 - (int)blockIdx.x;
                 h = blockIdx.y;
@@ -121,21 +128,26 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             }
             return k == 0;
         } else {
-            const long long G = gridDim.x, c = blockIdx.x;
-            const long long t = (long long)k * G + ((k & 1) ? G - 1 - c : c);
-            const long long BH = (long long)p.H * p.B;
-            if (t >= (long long)num_pairs * BH) return false;
-            long long bh, w;
+            // 32-bit index arithmetic (the launcher keeps the tile count
+            // below 2^30) with divisions by invariant multipliers: the
+            // softmax warps compute the next tile's indices between two
+            // tiles, where a division's latency delays the next scores.
+            const unsigned G = gridDim.x, c = blockIdx.x;
+            const unsigned t = (unsigned)k * G + ((k & 1) ? G - 1 - c : c);
+            const unsigned BH = (unsigned)p.H * (unsigned)p.B, NT = (unsigned)num_pairs;
+            if (t >= NT * BH) return false;
+            unsigned bh, w;
             if (p.weight_major) {   // as in the differential prefill
-                w = t / BH;
+                w = div_inv(t, p.div_major_m, p.div_major_s);
                 bh = t - w * BH;
             } else {
-                bh = t / num_pairs;
-                w = t - bh * num_pairs;
+                bh = div_inv(t, p.div_major_m, p.div_major_s);
+                w = t - bh * NT;
             }
             pr = num_pairs - 1 - (int)w;
-            h = (int)(bh % p.H);
-            b = (int)(bh / p.H);
+            const unsigned bb = div_inv(bh, p.div_h_m, p.div_h_s);
+            h = (int)(bh - bb * (unsigned)p.H);
+            b = (int)bb;
             return true;
         }
     };

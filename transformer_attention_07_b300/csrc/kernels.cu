@@ -88,6 +88,27 @@ static bool make_map_bhnd(CUtensorMap* m, const void* base, int B, int H, int N,
     return r == CUDA_SUCCESS;
 }
 
+// Launches a decode kernel as a dependent grid (programmatic stream
+// serialisation): it may be scheduled while the previous grid on the stream
+// drains, and waits for that grid's completion inside the kernel before it
+// touches memory.  The split and merge kernels of one call then follow each
+// other without a full launch gap.
+template <typename... Params, typename... Args>
+static cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 // ----------------------------------------------------------------- prefill
 
 // Streaming multiprocessors of the current device (0 if unknown), cached per
@@ -204,8 +225,10 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     const dim3 grid = persist          ? dim3(sms, 1, 1)
                       : p.head_group ? dim3((unsigned)tiles, 1, 1)
                                      : dim3((a.Nq + L::BM - 1) / L::BM, a.H, a.B);
-    kern<<<grid, L::THREADS, smem, st>>>(mq1, mq2, mk1, mk2, mv, mo, p);
-    return cuda_ok(cudaGetLastError(), "prefill: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+    return cuda_ok(launch_dependent(kern, grid, dim3(L::THREADS), (size_t)smem, st, mq1, mq2, mk1, mk2, mv, mo, p),
+                   "prefill: launch")
+               ? LAUNCH_OK
+               : LAUNCH_ERR_CUDA;
 }
 
 template <bool QK8>
@@ -365,8 +388,10 @@ static int launch_standard_t(const StandardArgs& a, cudaStream_t st) {
     const dim3 grid = persist          ? dim3(sms, 1, 1)
                       : p.head_group ? dim3((unsigned)pairs, 1, 1)
                                      : dim3((a.Nq + 2 * L::BM - 1) / (2 * L::BM), a.H, a.B);
-    kern<<<grid, L::THREADS, L::SMEM_BYTES, st>>>(mq, mk, mv, mo, p);
-    return cuda_ok(cudaGetLastError(), "standard attention: launch") ? LAUNCH_OK : LAUNCH_ERR_CUDA;
+    return cuda_ok(launch_dependent(kern, grid, dim3(L::THREADS), (size_t)L::SMEM_BYTES, st, mq, mk, mv, mo, p),
+                   "standard attention: launch")
+               ? LAUNCH_OK
+               : LAUNCH_ERR_CUDA;
 }
 
 int launch_standard(const StandardArgs& a, cudaStream_t st) {
@@ -376,26 +401,6 @@ int launch_standard(const StandardArgs& a, cudaStream_t st) {
 
 // ----------------------------------------------------------------- decode
 
-// Launches a decode kernel as a dependent grid (programmatic stream
-// serialisation): it may be scheduled while the previous grid on the stream
-// drains, and waits for that grid's completion inside the kernel before it
-// touches memory.  The split and merge kernels of one call then follow each
-// other without a full launch gap.
-template <typename... Params, typename... Args>
-static cudaError_t launch_dependent(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                                    Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
 
 template <int D, int DV, bool PAGED>
 static int launch_decode_t(const DecodeArgs& a, cudaStream_t st) {

@@ -191,6 +191,13 @@ standard_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + L::OFF_TMEM_SLOT);
+    // Launched as a dependent grid (programmatic stream serialisation): no
+    // global memory is read or written before the previous grid on the stream
+    // has completed, since its output may be this call's input.  The next
+    // grid may be scheduled from here on: its CTAs take SMs as this grid's
+    // CTAs leave and set up while the last of them finish.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer

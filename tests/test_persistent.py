@@ -1,6 +1,7 @@
 """GPU parity of the persistent grids (one CTA per SM walking the query tiles),
 which the prefill and the single-map kernel use for key lengths up to 4096
-when there are more query tiles than SMs.
+when there are more query tiles than SMs (the prefill also up to 8192 keys
+when its tile list is weight-major).
 
 Every shape here has more tiles than the B300's SMs, so the call runs the
 persistent form.  Two checks per shape:
@@ -12,8 +13,8 @@ persistent form.  Two checks per shape:
 The shapes cover ragged Nq < Nk, non-causal ragged keys, d = 32, and tile
 counts that end in a partial round after rounds in both directions.  Under
 causal masking the tile list is weight-major when every head's K and V fit
-in 64 MB together (the first, third and fourth shapes) and (b, h)-major
-otherwise (the fifth, 335 MB).
+in 64 MB together (the first, third, fourth and sixth shapes; the sixth has
+8192 keys) and (b, h)-major otherwise (the fifth, 335 MB).
 
 The one-tile form under causal masking runs a 1-D grid in weight order
 within groups of heads when at least four heads' K and V fit in 16 MB;
@@ -34,6 +35,15 @@ pytestmark = pytest.mark.gpu
 TOL_PRE = 1e-2
 TOL_OUT = 3e-2
 MAX_PERSIST_NK = 4096
+MAX_PERSIST_NK_WEIGHT_MAJOR = 8192
+WEIGHT_MAJOR_BYTES = 64 << 20
+
+
+def takes_persistent_form(B, H, Nq, Nk, d, dv, causal):
+    """The prefill launcher's choice, restated for the test's shapes."""
+    tiles = B * H * math.ceil(Nq / 128)
+    weight_major = causal and B * H * Nk * (4 * d + 2 * dv) <= WEIGHT_MAJOR_BYTES   # bf16 K1, K2 and V bytes
+    return tiles > sms() and (Nk <= MAX_PERSIST_NK or (weight_major and Nk <= MAX_PERSIST_NK_WEIGHT_MAJOR))
 
 
 def sms():
@@ -62,10 +72,10 @@ def boundary_rows(Nq):
     (3, 50, 640, 640, 64, 128, True),     # 750 tiles: five rounds in alternating directions, then a partial one
     (1, 160, 200, 200, 32, 64, True),     # d = 32, dv = 64; 320 tiles
     (4, 40, 640, 4096, 64, 128, True),    # 800 tiles, K/V 335 MB: the (b, h)-major list
+    (1, 16, 2000, 8192, 64, 128, True),   # 256 tiles, 8192 keys, K/V 64 MB: persistent through the weight-major list
 ])
 def test_persistent_prefill(B, H, Nq, Nk, d, dv, causal):
-    tiles = B * H * math.ceil(Nq / 128)
-    assert tiles > sms() and Nk <= MAX_PERSIST_NK, "shape would not take the persistent form"
+    assert takes_persistent_form(B, H, Nq, Nk, d, dv, causal), "shape would not take the persistent form"
     lam, lam_init, eps = 0.6, 0.8, 1e-5
     inp = random_inputs(B, H, Nq, Nk, d, dv, seed=Nq * 7 + Nk + H)
     pre = torch.full((B, H, Nq, dv), float("nan"), dtype=torch.float32, device="cuda")
@@ -128,7 +138,7 @@ def test_persistent_single_map_kernel():
 def test_grouped_one_tile_grid(B, H, Nq, Nk):
     d, dv = 64, 128
     tiles = B * H * math.ceil(Nq / 128)
-    assert tiles <= sms() or Nk > MAX_PERSIST_NK, "shape would take the persistent form"
+    assert not takes_persistent_form(B, H, Nq, Nk, d, dv, True), "shape would take the persistent form"
     assert (16 << 20) // (Nk * (2 * d + dv) * 2) >= 4, "fewer than four heads per group"
     lam, lam_init, eps = 0.6, 0.8, 1e-5
     inp = random_inputs(B, H, Nq, Nk, d, dv, seed=Nq + Nk + 5 * H)

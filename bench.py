@@ -530,7 +530,7 @@ def run_cuda(args, world, rank, local):
     # at 350-450 W) for seconds, idle or not, and a 60 us kernel then takes
     # up to a quarter longer; each short case records the clock it saw.
     early = {}
-    if args.only == "all" and not args.no_compare:
+    if args.only == "all" and not args.no_compare and rank == 0:   # reported by rank 0 only
         early["single_map_baseline"] = compare_single_map(dev)
         early["decode_small_latency"] = small_decode_latency(dev)
         early["prefill_by_length"] = prefill_by_length(dev, names=SHORT_LENGTHS)

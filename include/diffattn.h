@@ -82,6 +82,34 @@ int diffattn_fwd_ex(const void* q1, const void* k1, const void* q2, const void* 
                     const float* gn_gamma, float eps, void* out, float* o_prenorm, void* stream);
 
 /*
+ * How diffattn_fwd, diffattn_fwd_ex, diffattn_fwd_train and diffattn_fwd_fp8
+ * (fp8 = 1) launch the prefill for a shape on a device with `sms` streaming
+ * multiprocessors (148 on a B300).  The operation is the one diffattn_fwd
+ * computes (iloveeagents.com Q&A, "Mathematical Formula"); how its query
+ * tiles of 128 rows are spread over the GPU is this library's own.  Pure
+ * host arithmetic, no CUDA call; every form gives the same bits.
+ *   *form  DIFFATTN_PLAN_TILE_GRID (0): one CTA per query tile, grid (tile, h, b)
+ *          DIFFATTN_PLAN_TILE_GROUPED (1): one CTA per query tile, a 1-D grid
+ *            in weight order within groups of heads (causal, K and V of at
+ *            least four heads fit in 16 MB)
+ *          DIFFATTN_PLAN_PERSISTENT (2): one CTA per SM walking a (b, h)-major
+ *            tile list (more tiles than SMs, Nk <= 4096)
+ *          DIFFATTN_PLAN_PERSISTENT_WEIGHT (3): the same over a weight-major
+ *            list (causal, all heads' K and V within 64 MB; Nk <= 8192)
+ *   *ctas  CTAs launched (0 for an empty problem)
+ * Returns DIFFATTN_ERR_INVALID_ARG for bad sizes, sms < 1 or null outputs,
+ * DIFFATTN_ERR_UNSUPPORTED for a (d, dv) pair without a kernel.
+ */
+enum {
+    DIFFATTN_PLAN_TILE_GRID = 0,
+    DIFFATTN_PLAN_TILE_GROUPED = 1,
+    DIFFATTN_PLAN_PERSISTENT = 2,
+    DIFFATTN_PLAN_PERSISTENT_WEIGHT = 3
+};
+int diffattn_prefill_plan(int B, int H, int Nq, int Nk, int d, int dv, int causal, int fp8, int sms, int* form,
+                          long long* ctas);
+
+/*
  * Prefill forward with 8-bit queries and keys.  The pages link differential
  * attention to low-bit quantisation through its smaller activation outliers
  * (llmbytes.dev, "Quantization Friendliness").  Here q1, k1, q2, k2 are

@@ -33,7 +33,7 @@ def test_header_declares_the_entry_points():
     assert declared_functions() == sorted([
         "diffattn_fwd", "diffattn_fwd_ex", "diffattn_fwd_host", "diffattn_fwd_host_workspace_bytes", "diffattn_fwd_fp8",
         "diffattn_fwd_train", "diffattn_bwd_workspace_bytes", "diffattn_bwd",
-        "diffattn_decode_workspace_bytes", "diffattn_decode_auto_splits", "diffattn_decode", "diffattn_decode_partials_bytes",
+        "diffattn_decode_workspace_bytes", "diffattn_decode_auto_splits", "diffattn_prefill_plan", "diffattn_decode", "diffattn_decode_partials_bytes",
         "diffattn_decode_partials", "diffattn_decode_merge",
         "diffattn_decode_noalloc", "diffattn_decode_paged", "diffattn_standard_fwd", "diffattn_status_string",
         "diffattn_last_device_error", "diffattn_selftest_wait_timeout"])

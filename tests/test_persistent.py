@@ -34,16 +34,9 @@ pytestmark = pytest.mark.gpu
 
 TOL_PRE = 1e-2
 TOL_OUT = 3e-2
-MAX_PERSIST_NK = 4096
-MAX_PERSIST_NK_WEIGHT_MAJOR = 8192
-WEIGHT_MAJOR_BYTES = 64 << 20
-
-
-def takes_persistent_form(B, H, Nq, Nk, d, dv, causal):
-    """The prefill launcher's choice, restated for the test's shapes."""
-    tiles = B * H * math.ceil(Nq / 128)
-    weight_major = causal and B * H * Nk * (4 * d + 2 * dv) <= WEIGHT_MAJOR_BYTES   # bf16 K1, K2 and V bytes
-    return tiles > sms() and (Nk <= MAX_PERSIST_NK or (weight_major and Nk <= MAX_PERSIST_NK_WEIGHT_MAJOR))
+def plan_form(B, H, Nq, Nk, d, dv, causal):
+    """The launch form the prefill entry points take on this device."""
+    return da.prefill_plan(B, H, Nq, Nk, d, dv, causal=causal, sms=sms())[0]
 
 
 def sms():
@@ -66,16 +59,16 @@ def boundary_rows(Nq):
     return sorted(r for r in rows if 0 <= r < Nq)
 
 
-@pytest.mark.parametrize("B,H,Nq,Nk,d,dv,causal", [
-    (1, 80, 300, 1000, 64, 128, True),    # Nq < Nk, ragged rows; 240 tiles
-    (2, 50, 256, 777, 64, 128, False),    # non-causal, ragged keys; 200 tiles
-    (3, 50, 640, 640, 64, 128, True),     # 750 tiles: five rounds in alternating directions, then a partial one
-    (1, 160, 200, 200, 32, 64, True),     # d = 32, dv = 64; 320 tiles
-    (4, 40, 640, 4096, 64, 128, True),    # 800 tiles, K/V 335 MB: the (b, h)-major list
-    (1, 16, 2000, 8192, 64, 128, True),   # 256 tiles, 8192 keys, K/V 64 MB: persistent through the weight-major list
+@pytest.mark.parametrize("B,H,Nq,Nk,d,dv,causal,form", [
+    (1, 80, 300, 1000, 64, 128, True, "persistent_weight"),    # Nq < Nk, ragged rows; 240 tiles
+    (2, 50, 256, 777, 64, 128, False, "persistent"),           # non-causal, ragged keys; 200 tiles
+    (3, 50, 640, 640, 64, 128, True, "persistent_weight"),     # 750 tiles: five rounds in alternating directions, then a partial one
+    (1, 160, 200, 200, 32, 64, True, "persistent_weight"),     # d = 32, dv = 64; 320 tiles
+    (4, 40, 640, 4096, 64, 128, True, "persistent"),           # 800 tiles, K/V 335 MB: the (b, h)-major list
+    (1, 16, 2000, 8192, 64, 128, True, "persistent_weight"),   # 256 tiles, 8192 keys, K/V 64 MiB
 ])
-def test_persistent_prefill(B, H, Nq, Nk, d, dv, causal):
-    assert takes_persistent_form(B, H, Nq, Nk, d, dv, causal), "shape would not take the persistent form"
+def test_persistent_prefill(B, H, Nq, Nk, d, dv, causal, form):
+    assert plan_form(B, H, Nq, Nk, d, dv, causal) == form
     lam, lam_init, eps = 0.6, 0.8, 1e-5
     inp = random_inputs(B, H, Nq, Nk, d, dv, seed=Nq * 7 + Nk + H)
     pre = torch.full((B, H, Nq, dv), float("nan"), dtype=torch.float32, device="cuda")
@@ -137,9 +130,7 @@ def test_persistent_single_map_kernel():
 ])
 def test_grouped_one_tile_grid(B, H, Nq, Nk):
     d, dv = 64, 128
-    tiles = B * H * math.ceil(Nq / 128)
-    assert not takes_persistent_form(B, H, Nq, Nk, d, dv, True), "shape would take the persistent form"
-    assert (16 << 20) // (Nk * (2 * d + dv) * 2) >= 4, "fewer than four heads per group"
+    assert plan_form(B, H, Nq, Nk, d, dv, True) == "tile_grouped"
     lam, lam_init, eps = 0.6, 0.8, 1e-5
     inp = random_inputs(B, H, Nq, Nk, d, dv, seed=Nq + Nk + 5 * H)
     out = da.fwd(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], lam, lam_init, causal=True,

@@ -19,7 +19,8 @@ import os
 
 __all__ = [
     "fwd", "fwd_host", "fwd_host_workspace_bytes", "fwd_fp8", "fwd_train", "bwd", "bwd_workspace_bytes",
-    "standard_fwd", "decode", "decode_paged", "decode_workspace_bytes", "decode_auto_splits", "decode_partials", "decode_partials_bytes",
+    "standard_fwd", "decode", "decode_paged", "decode_workspace_bytes", "decode_auto_splits", "prefill_plan", "PLAN_FORMS",
+    "decode_partials", "decode_partials_bytes",
     "decode_merge", "gather_partials", "decode_sharded", "head_range", "gather_heads", "fwd_sharded",
     "status_string", "last_device_error", "selftest_wait_timeout", "load", "LIB_PATH",
     "DiffAttnError", "SUPPORTED_WIDTHS",
@@ -59,6 +60,9 @@ def load():
     lib.diffattn_decode_workspace_bytes.restype = sz
     lib.diffattn_decode_auto_splits.argtypes = [i32, i32, i32, i32, i32, i32, i32]
     lib.diffattn_decode_auto_splits.restype = i32
+    lib.diffattn_prefill_plan.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int),
+                                          ctypes.POINTER(ctypes.c_longlong)]
+    lib.diffattn_prefill_plan.restype = i32
     lib.diffattn_decode.argtypes = [vp, vp, vp, vp, vp, f32, f32, i32, i32, i32, i32, i32, vp, f32, i32, vp, sz,
                                     vp, vp, vp]
     lib.diffattn_decode.restype = i32
@@ -297,6 +301,20 @@ def standard_fwd(q, k, v, causal=False, out=None, out_f32=None, stream=None):
 
 def decode_workspace_bytes(B, H, Nk, dv, num_splits=0) -> int:
     return int(load().diffattn_decode_workspace_bytes(B, H, Nk, dv, num_splits))
+
+
+PLAN_FORMS = ("tile_grid", "tile_grouped", "persistent", "persistent_weight")
+
+
+def prefill_plan(B, H, Nq, Nk, d=64, dv=128, causal=True, fp8=False, sms=148):
+    """How the prefill entry points launch this shape on a device with ``sms``
+    SMs (host arithmetic): returns (form, ctas), form one of PLAN_FORMS."""
+    form, ctas = ctypes.c_int(-1), ctypes.c_longlong(-1)
+    rc = load().diffattn_prefill_plan(B, H, Nq, Nk, d, dv, int(bool(causal)), int(bool(fp8)), sms,
+                                      ctypes.byref(form), ctypes.byref(ctas))
+    if rc != OK:
+        raise DiffAttnError(rc, "diffattn_prefill_plan")
+    return PLAN_FORMS[form.value], int(ctas.value)
 
 
 def decode_auto_splits(B, H, Nk, d, dv, sms, max_splits=0) -> int:

@@ -236,6 +236,19 @@ int diffattn_standard_fwd(const void* q, const void* k, const void* v, int causa
     return from_launch(diffattn::launch_standard(a, static_cast<cudaStream_t>(stream)));
 }
 
+int diffattn_prefill_plan(int B, int H, int Nq, int Nk, int d, int dv, int causal, int fp8, int sms, int* form,
+                          long long* ctas) {
+    if (form == nullptr || ctas == nullptr) return DIFFATTN_ERR_INVALID_ARG;
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 1 || sms < 1 || (causal != 0 && causal != 1) || (fp8 != 0 && fp8 != 1))
+        return DIFFATTN_ERR_INVALID_ARG;
+    if (causal && Nq > Nk) return DIFFATTN_ERR_INVALID_ARG;
+    if (!supported_widths(d, dv)) return DIFFATTN_ERR_UNSUPPORTED;
+    const diffattn::PrefillPlan pl = diffattn::prefill_plan(B, H, Nq, Nk, d, dv, causal != 0, fp8 != 0, sms);
+    *form = pl.form;
+    *ctas = pl.ctas;
+    return DIFFATTN_OK;
+}
+
 int diffattn_decode_auto_splits(int B, int H, int Nk, int d, int dv, int sms, int max_splits) {
     if (B < 1 || H < 1 || Nk < 1 || sms < 1 || max_splits < 0 || max_splits > kMaxSplits) return 0;
     if (!supported_widths(d, dv)) return 0;

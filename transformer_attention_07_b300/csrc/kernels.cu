@@ -182,6 +182,23 @@ static int head_group_size(int B, int H, int Nk, long long bytes_per_key) {
     return g >= 4 ? (int)g : 0;
 }
 
+PrefillPlan prefill_plan(int B, int H, int Nq, int Nk, int d, int dv, bool causal, bool qk8, int sms) {
+    constexpr int BM = 128;   // query rows per tile (PrefillLayout::BM)
+    const long long bytes_per_key = 2ll * d * (qk8 ? 1 : 2) + 2ll * dv;
+    const long long num_qt = (Nq + BM - 1) / BM;
+    const long long tiles = num_qt * H * B;
+    PrefillPlan pl;
+    pl.weight_major = weight_major_order(causal, B, H, Nk, bytes_per_key);
+    // Both 1-D orders index their tiles with 32-bit arithmetic.
+    const bool small = tiles < kMaxTiles1D;
+    const bool persist = sms > 0 && tiles > sms && small &&
+                         (Nk <= kPersistMaxNk || (pl.weight_major && Nk <= kPersistMaxNkWeightMajor));
+    pl.head_group = causal && !persist && small ? head_group_size(B, H, Nk, bytes_per_key) : 0;
+    pl.form = persist ? (pl.weight_major ? 3 : 2) : pl.head_group > 0 ? 1 : 0;
+    pl.ctas = persist ? sms : tiles;
+    return pl;
+}
+
 template <int D, int DV, bool CAUSAL, bool QK8>
 static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     using L = PrefillLayout<D, DV, QK8>;
@@ -214,17 +231,15 @@ static int launch_prefill_t(const PrefillArgs& a, cudaStream_t st) {
     p.o2 = a.o2;
     p.lse = a.lse;
     p.qk_scale = a.qk_scale;
-    p.weight_major = weight_major_order(CAUSAL, a.B, a.H, a.Nk, 2ll * D * qe + 2ll * DV);
     const long long tiles = (long long)((a.Nq + L::BM - 1) / L::BM) * a.H * a.B;
     const int sms = sm_count();
-    // Both 1-D orders index their tiles with 32-bit arithmetic.
-    const bool small = tiles < kMaxTiles1D;
-    const bool persist = sms > 0 && tiles > sms && small &&
-                         (a.Nk <= kPersistMaxNk || (p.weight_major && a.Nk <= kPersistMaxNkWeightMajor));
+    const PrefillPlan plan = prefill_plan(a.B, a.H, a.Nq, a.Nk, D, DV, CAUSAL, QK8, sms);
+    p.weight_major = plan.weight_major;
+    const bool persist = plan.form >= 2;
     inv_div(p.weight_major ? (unsigned)((long long)a.H * a.B) : (unsigned)((a.Nq + L::BM - 1) / L::BM), p.div_major_m,
             p.div_major_s);
     inv_div((unsigned)a.H, p.div_h_m, p.div_h_s);
-    p.head_group = CAUSAL && !persist && small ? head_group_size(a.B, a.H, a.Nk, 2ll * D * qe + 2ll * DV) : 0;
+    p.head_group = plan.head_group;
     auto kern = persist ? prefill_kernel<D, DV, CAUSAL, QK8, true> : prefill_kernel<D, DV, CAUSAL, QK8, false>;
     const int smem = (int)(persist ? PrefillLayout<D, DV, QK8, true>::SMEM_BYTES : L::SMEM_BYTES);
     if (!cuda_ok(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem),

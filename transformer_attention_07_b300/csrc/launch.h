@@ -83,6 +83,19 @@ struct BwdWorkspace {
 };
 BwdWorkspace bwd_workspace_layout(int B, int H, int Nq, int dv);
 
+// How the prefill is launched for a shape on a device with `sms` SMs (host
+// arithmetic; the launcher uses exactly this).  form: 0 = one CTA per query
+// tile on the (tile, h, b) grid, 1 = one CTA per query tile on a 1-D grid in
+// weight order within head groups, 2 = persistent grid over a (b, h)-major
+// tile list, 3 = persistent grid over a weight-major list.
+struct PrefillPlan {
+    int form;
+    long long ctas;     // CTAs launched
+    int weight_major;   // the persistent list's order (kernel parameter)
+    int head_group;     // heads per group of form 1, else 0 (kernel parameter)
+};
+PrefillPlan prefill_plan(int B, int H, int Nq, int Nk, int d, int dv, bool causal, bool qk8, int sms);
+
 int launch_prefill(const PrefillArgs& a, cudaStream_t st);
 int launch_backward(const BwdArgs& a, cudaStream_t st);
 int launch_standard(const StandardArgs& a, cudaStream_t st);
